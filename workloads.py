@@ -1,0 +1,102 @@
+"""Seeded synthetic workloads shared by the tests, ``bench.py`` and ``smoke()``.
+
+This module holds input shapes and random draws only: no attention arithmetic.
+Both the CUDA path and the CPU oracle consume the tensors made here.
+
+Recipe (one per workload): a CPU ``torch.Generator`` seeded with
+``1000 + index`` draws Q, K, V, dO in that order as fp32 standard normals of
+shape ``[B, H, N, d]``; each is rounded once to bf16 (round to nearest even).
+The GPU receives those bf16 tensors; the oracle receives the same values
+upcast to float64, so parity measures kernel error, not input quantisation.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int          # seed = 1000 + index
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    backward: bool = True
+    note: str = ""
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def seed(self) -> int:
+        return 1000 + self.index
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "H": self.H, "N": self.N, "d": self.d,
+                "causal": self.causal, "scale": "1/sqrt(d)", "backward": self.backward}
+
+
+# The five workloads the method is measured and checked on.
+TINY = Workload("tiny_b1_h2_n256_d64", 0, 1, 2, 256, 64, False, True,
+                "fwd+bwd, no mask; small enough for a full oracle in seconds")
+GPT2_MEDIUM = Workload("gpt2_medium_b64_h16_n1024_d64_causal", 1, 64, 16, 1024, 64, True, True,
+                       "GPT-2 medium attention shape (blog.teqners.com opening benchmark), fwd+bwd")
+LLAMA7B_LAYER = Workload("7b_layer_b1_h32_n4096_d128_causal", 2, 1, 32, 4096, 128, True, False,
+                         "7B-layer attention shape, forward only")
+LLAMA7B_LAYER_NC = Workload("7b_layer_b1_h32_n4096_d128", 2, 1, 32, 4096, 128, False, False,
+                            "7B-layer attention shape, forward only, no mask")
+LONG_SEQ = Workload("long_b1_h16_n16384_d128", 3, 1, 16, 16384, 128, False, True,
+                    "long sequence, small batch: work is split along the sequence")
+
+
+def sweep() -> list[Workload]:
+    """B*N fixed at 16384 tokens, H = 16, N in 512..16384, d in {64, 128}, both masks."""
+    out = []
+    for d in (64, 128):
+        for causal in (False, True):
+            for n in (512, 1024, 2048, 4096, 8192, 16384):
+                out.append(Workload(f"sweep_b{16384 // n}_h16_n{n}_d{d}{'_causal' if causal else ''}",
+                                    4, 16384 // n, 16, n, d, causal, True))
+    return out
+
+
+ALL = [TINY, GPT2_MEDIUM, LLAMA7B_LAYER, LLAMA7B_LAYER_NC, LONG_SEQ]
+BY_NAME = {w.name: w for w in ALL + sweep()}
+
+
+def make_inputs(B, H, N, d, seed, stress=None):
+    """Seeded bf16 Q, K, V, dO of shape [B, H, N, d] on the CPU.
+
+    ``stress``: ``None`` for plain N(0, 1); ``"wide"`` multiplies Q by 8 so score
+    rows span dozens of units (exercises running-max growth and rescaling);
+    ``"spike"`` additionally plants one large key per query block; ``"sorted"``
+    sorts keys so each row's maximum keeps growing along the sequence.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    do = torch.randn(shape, generator=g, dtype=torch.float32)
+    if stress in ("wide", "spike", "sorted"):
+        q = q * 8.0
+    if stress == "spike":
+        idx = torch.randint(0, N, (B, H), generator=g)
+        for b in range(B):
+            for h in range(H):
+                k[b, h, idx[b, h]] *= 6.0
+    if stress == "sorted":
+        k, _ = torch.sort(k, dim=2)
+    return tuple(t.to(torch.bfloat16) for t in (q, k, v, do))
+
+
+def workload_inputs(w: Workload, stress=None):
+    return make_inputs(w.B, w.H, w.N, w.d, w.seed, stress)
