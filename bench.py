@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Throughput of exact fused attention (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch of the workload: the
+forward (one launch) and, for workloads with a backward, the backward's three
+launches (preprocess, fused dK/dV/dQ, dQ convert), all through the C ABI.
+FLOPs per step use the library's formula: 4 B H N^2 d for the forward, halved
+under the causal mask, and 2.5 times that for the backward.
+
+Prints ONE JSON line (rank 0).  ``value`` is device-timed TFLOP/s over all
+ranks with inputs resident in HBM; ``e2e`` is the same metric through the
+same C ABI with pinned host buffers copied in and results copied out inside
+the timed region; ``roofline`` reports the dominant kernel against the
+measured bf16 peak; ``cpu_baseline`` times the fp64 CPU oracle on a bounded
+sample.  Under torchrun each rank runs an independent replica of the
+workload on its own GPU (no collective on the data path; weak scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s and % of GB300 dense BF16 peak (1 GPU)"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CSRC = os.path.join(ROOT, "exact_io_aware_31_gb300", "csrc")
+
+
+def flops_per_step(w):
+    f = 4.0 * w.B * w.H * w.N * w.N * w.d
+    if w.causal:
+        f /= 2
+    fwd = f
+    bwd = 2.5 * f if w.backward else 0.0
+    return fwd, bwd
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel, workload):
+    """Bytes per launch from a committed ncu capture, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    rec = table.get(kernel, {}).get(workload)
+    if not rec or rec.get("source_sha") != source_hash():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sms.append(float(parts[0]))
+                    maxes.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[3:7]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+def oracle_sample(w, q, k, v, do, seconds):
+    """Time the fp64 oracle (forward + backward) on whole (b, h) slices for about `seconds`."""
+    import oracle
+    fwd, bwd = flops_per_step(w)
+    per_slice = (fwd + bwd) / (w.B * w.H)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        b, h = divmod(done % (w.B * w.H), w.H)
+        qd, kd, vd, dod = (t[b, h].double().numpy() for t in (q, k, v, do))
+        if w.backward:
+            oracle.attention_backward_head(qd, kd, vd, dod, w.scale, w.causal)
+        else:
+            oracle.attention_forward_head_rows(qd, kd, vd, range(w.N), w.scale, w.causal)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return done * per_slice / el / 1e12, done, el
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    q, k, v, do = workloads.workload_inputs(w)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        val, n, el = oracle_sample(w, q, k, v, do, args.ref_seconds)
+        if i >= args.warmup:
+            vals.append((val, n, el))
+    value = statistics.median(v for v, _, _ in vals)
+    fwd, bwd = flops_per_step(w)
+    sample = (f"whole (b,h) slices of the workload, fwd{'+bwd' if w.backward else ''} in fp64 numpy, "
+              f"about {args.ref_seconds:.0f} s per step ({vals[-1][1]} slices of {w.B * w.H} in the last)")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * (fwd + bwd) / (value * 1e12), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {**w.describe(), "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import exact_io_aware_31_gb300 as fa
+    from exact_io_aware_31_gb300 import build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    fa.load_library()
+
+    q, k, v, do = workloads.workload_inputs(w)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    dev = torch.device("cuda", local)
+    qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qg)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(qg) for _ in range(3))
+    ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    scale, causal = w.scale, int(w.causal)
+    in_bytes = qg.numel() * 2
+    flush = in_bytes < L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+
+    def check(st, where):
+        if st != fa.FA_OK:
+            raise fa.FaError(st, where)
+
+    def step(ev):
+        ev[0].record(stream)
+        check(fa.fa_fwd(qg.data_ptr(), kg.data_ptr(), vg.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                        scale, causal, sh), "fa_fwd")
+        ev[1].record(stream)
+        if w.backward:
+            check(fa.fa_bwd_preprocess(o.data_ptr(), dog.data_ptr(), lse.data_ptr(), B, H, N, d, ws.data_ptr(),
+                                       ws_bytes, sh), "fa_bwd_preprocess")
+            ev[2].record(stream)
+            check(fa.fa_bwd_dkdv(qg.data_ptr(), kg.data_ptr(), vg.data_ptr(), dog.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), B, H, N, d, scale, causal, ws.data_ptr(), ws_bytes, sh),
+                  "fa_bwd_dkdv")
+            ev[3].record(stream)
+            check(fa.fa_bwd_dq_convert(dq.data_ptr(), B, H, N, d, scale, ws.data_ptr(), ws_bytes, sh),
+                  "fa_bwd_dq_convert")
+            ev[4].record(stream)
+
+    launches_per_step = 4 if w.backward else 1
+    nev = 5 if w.backward else 2
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(nev)])
+        if flush:
+            flush_buf.zero_()
+    torch.cuda.synchronize()
+    check(fa.fa_get_device_status(sh), "warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    # Clock samples: nvidia-smi samples every 100 ms, longer than a short timed
+    # region, so identical untimed steps keep the GPU busy for about half a
+    # second before it and the samples cover that window plus the region.
+    sampler = ClockSampler(local)
+    sampler.start()
+    spare = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+    t_busy = time.perf_counter()
+    busy_steps = 0
+    while time.perf_counter() - t_busy < 0.6:
+        step(spare)
+        busy_steps += 1
+        if busy_steps % 8 == 0:
+            torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    region0.record(stream)
+    for i in range(args.steps):
+        step(events[i])
+        if flush and i + 1 < args.steps:
+            flush_buf.zero_()   # outside the per-step events
+    region1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    if clocks is not None:
+        clocks["window"] = f"{busy_steps} untimed identical steps, then the timed region"
+    check(fa.fa_get_device_status(sh), "timed region")
+
+    step_ms = [e[0].elapsed_time(e[nev - 1]) for e in events]
+    ms_per_step = sum(step_ms) / args.steps if flush else region0.elapsed_time(region1) / args.steps
+    kern = {"fa_fwd_kernel": [e[0].elapsed_time(e[1]) for e in events]}
+    if w.backward:
+        kern["fa_bwd_pre"] = [e[1].elapsed_time(e[2]) for e in events]
+        kern["fa_bwd_main"] = [e[2].elapsed_time(e[3]) for e in events]
+        kern["fa_bwd_dq_conv"] = [e[3].elapsed_time(e[4]) for e in events]
+    kern_avg = {k_: sum(v_) / len(v_) for k_, v_ in kern.items()}
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+
+    fwd_f, bwd_f = flops_per_step(w)
+    value = world * (fwd_f + bwd_f) / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end: pinned host buffers in, results out, same C ABI ----
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    hdq, hdk, hdv = (torch.empty(q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3))
+    outs_h = [ho, hlse] + ([hdq, hdk, hdv] if w.backward else [])
+    outs_d = [o, lse] + ([dq, dk, dv] if w.backward else [])
+    h2d = sum(t.numel() * t.element_size() for t in ((hq, hk, hv, hdo) if w.backward else (hq, hk, hv)))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for hd, dd in ((hq, qg), (hk, kg), (hv, vg)) + (((hdo, dog),) if w.backward else ()):
+            dd.copy_(hd, non_blocking=True)
+        check(fa.fa_fwd(qg.data_ptr(), kg.data_ptr(), vg.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                        scale, causal, sh), "fa_fwd")
+        if w.backward:
+            check(fa.fa_bwd(qg.data_ptr(), kg.data_ptr(), vg.data_ptr(), o.data_ptr(), dog.data_ptr(),
+                            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, causal,
+                            ws.data_ptr(), ws_bytes, sh), "fa_bwd")
+        for hd, dd in zip(outs_h, outs_d):
+            hd.copy_(dd, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12
+    check(fa.fa_get_device_status(sh), "e2e")
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel ----
+    peaks, peak_src = load_peaks()
+    dom = max(kern_avg, key=kern_avg.get)
+    per_launch = {"fa_fwd_kernel": fwd_f, "fa_bwd_main": bwd_f}
+    if dom in per_launch:
+        achieved = per_launch[dom] / (kern_avg[dom] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4)}
+    else:
+        bytes_ = (2 * w.B * w.H * w.N * w.d * 2 + 8 * w.B * w.H * w.N if dom == "fa_bwd_pre"
+                  else w.B * w.H * w.N * w.d * 6)
+        achieved = bytes_ / (kern_avg[dom] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4)}
+    roof["traffic"] = dram_traffic(dom, w.name)
+    roof["peak_source"] = f"{peak_src} (burst bf16 GEMM)" if roof["bound"] == "tensor" else peak_src
+    roof["kernel_ms"] = {k_: round(v_, 4) for k_, v_ in kern_avg.items()}
+    roof["kernel_frac_of_peak"] = {
+        k_: round(per_launch[k_] / (kern_avg[k_] * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)
+        for k_ in kern_avg if k_ in per_launch}
+
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {**w.describe(), "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": ("flushed between steps (2x L2 buffer written)" if flush
+                              else "inputs larger than L2 (each tensor > 129 MB)"),
+                       "fwd_tflop_per_step": round(fwd_f / 1e12, 4), "bwd_tflop_per_step": round(bwd_f / 1e12, 4),
+                       "pct_of_dense_bf16_2250": round(100 * value / world / 2250.0, 2),
+                       "pct_of_measured_bf16": round(100 * value / world / peaks["bf16_tflops"], 2)},
+            "roofline": roof, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+            "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps}}
+    if world == 1 and not args.no_cpu_baseline:
+        val, n, el = oracle_sample(w, q, k, v, do, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(val, 6), "unit": UNIT, "cores": cores(), "kind": "oracle",
+                                "sample": f"{n} whole (b,h) slice(s) of {w.B * w.H}, fwd"
+                                          f"{'+bwd' if w.backward else ''} in fp64 numpy, {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.GPT2_MEDIUM.name,
+                    help="one of: " + ", ".join(sorted(workloads.BY_NAME)))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
+    ap.add_argument("--ref-seconds", type=float, default=None,
+                    help="oracle time per step for --impl reference (default: 150 s spread over all steps)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "ours":
+        args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.ref_seconds is None:
+        args.ref_seconds = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    w = workloads.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

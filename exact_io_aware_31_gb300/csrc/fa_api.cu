@@ -1,0 +1,309 @@
+// The C ABI of include/fa.h: argument validation, TMA tensor maps, the device
+// status word, and kernel launches.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+
+namespace fa {
+
+// One status word per device that loads this library.  Kernels write
+// FA_ERR_DEVICE_TIMEOUT here when a bounded wait gives up.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  bool sm103 = false;
+  int* status = nullptr;  // device address of g_device_status
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Resolve per-device facts once, with that device current.
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+    d.sm103 = (major == 10 && minor == 3);
+    d.sms = sms;
+    if (d.sm103) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+      }
+      d.status = static_cast<int*>(p);
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  if (!d.sm103) return FA_ERR_UNSUPPORTED;
+  *out = &d;
+  return FA_OK;
+}
+
+// [B*H, N, d] bf16 viewed as a 3-D tensor; 128-row x 64-column boxes,
+// 128-byte swizzle (the layout the tcgen05 descriptors expect).
+int make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_sizes(int B, int H, int N, int d, float scale, int causal) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  if (bh > INT_MAX || (long long)N > (1 << 30)) return FA_ERR_INVALID_ARG;
+  const long long npad = ((long long)N + 127) / 128 * 128;
+  if (bh * npad * (d > 0 ? d : 1) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WorkspaceLayout {
+  size_t dq_acc, lse2, dsum, total;
+};
+
+WorkspaceLayout workspace_layout(int B, int H, int N, int d) {
+  const size_t bh = (size_t)B * H;
+  const size_t npad = ((size_t)N + 127) / 128 * 128;
+  WorkspaceLayout w;
+  w.dq_acc = 0;
+  w.lse2 = round256(bh * (size_t)N * d * 4);
+  w.dsum = w.lse2 + round256(bh * npad * 4);
+  w.total = w.dsum + round256(bh * npad * 4);
+  return w;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                      float scale, int causal, cudaStream_t stream) {
+  int st = check_sizes(B, H, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (make_map(&tq, q, BH, N, d) || make_map(&tk, k, BH, N, d) || make_map(&tv, v, BH, N, d)) return FA_ERR_CUDA;
+  FwdLaunch a;
+  a.tm_q = &tq;
+  a.tm_k = &tk;
+  a.tm_v = &tv;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.c2 = scale * 1.4426950408889634f;
+  a.status = dev->status;
+  const int units = fwd_units(BH, N);
+  a.grid = units < dev->sms ? units : dev->sms;
+  if (launch_fwd(a, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_sizes(B, H, N, d, 1.0f, 0) != FA_OK) return 0;
+  return workspace_layout(B, H, N, d).total;
+}
+
+namespace fa {
+namespace {
+
+// Validation and launch arguments shared by fa_bwd and its three phases.
+// `need` selects which tensor pointers the caller must supply.
+enum : unsigned { kNeedQKV = 1, kNeedO = 2, kNeedDout = 4, kNeedLse = 8, kNeedDq = 16, kNeedDkDv = 32 };
+
+int prepare_bwd(BwdLaunch& a, CUtensorMap* maps, unsigned need, const void* q, const void* k, const void* v,
+                const void* o, const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N,
+                int d, float scale, int causal, const void* workspace, size_t workspace_bytes) {
+  int st = check_sizes(B, H, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (((need & kNeedQKV) && (!aligned16(q) || !aligned16(k) || !aligned16(v))) ||
+      ((need & kNeedO) && !aligned16(o)) || ((need & kNeedDout) && !aligned16(dout)) ||
+      ((need & kNeedLse) && !aligned16(lse)) || ((need & kNeedDq) && !aligned16(dq)) ||
+      ((need & kNeedDkDv) && (!aligned16(dk) || !aligned16(dv))))
+    return FA_ERR_INVALID_ARG;
+  const WorkspaceLayout w = workspace_layout(B, H, N, d);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return FA_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const int BH = B * H;
+  if (need & kNeedQKV) {
+    if (make_map(&maps[0], q, BH, N, d) || make_map(&maps[1], k, BH, N, d) || make_map(&maps[2], v, BH, N, d) ||
+        make_map(&maps[3], dout, BH, N, d))
+      return FA_ERR_CUDA;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(const_cast<void*>(workspace));
+  a.tm_q = &maps[0];
+  a.tm_k = &maps[1];
+  a.tm_v = &maps[2];
+  a.tm_do = &maps[3];
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  a.dsum = reinterpret_cast<float*>(ws + w.dsum);
+  a.BH = BH;
+  a.N = N;
+  a.Npad = (N + 127) / 128 * 128;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.c2 = scale * 1.4426950408889634f;
+  a.status = dev->status;
+  const int units = bwd_units(BH, N);
+  a.grid = units < dev->sms ? units : dev->sms;
+  a.pre_grid = dev->sms * 8;
+  return FA_OK;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FA_OK;
+  cudaGetLastError();
+  return FA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                      void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  BwdLaunch a;
+  CUtensorMap maps[4];
+  int st = prepare_bwd(a, maps, kNeedQKV | kNeedO | kNeedDout | kNeedLse | kNeedDq | kNeedDkDv, q, k, v, o, dout,
+                       lse, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  if ((st = cuda_status(launch_bwd_pre(a, stream))) != FA_OK) return st;
+  if ((st = cuda_status(launch_bwd_main(a, stream))) != FA_OK) return st;
+  return cuda_status(launch_bwd_conv(a, stream));
+}
+
+extern "C" int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  BwdLaunch a;
+  CUtensorMap maps[4];
+  int st = prepare_bwd(a, maps, kNeedO | kNeedDout | kNeedLse, nullptr, nullptr, nullptr, o, dout, lse, nullptr,
+                       nullptr, nullptr, B, H, N, d, 1.0f, 0, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  return cuda_status(launch_bwd_pre(a, stream));
+}
+
+extern "C" int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv, int B,
+                           int H, int N, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  BwdLaunch a;
+  CUtensorMap maps[4];
+  int st = prepare_bwd(a, maps, kNeedQKV | kNeedDout | kNeedDkDv, q, k, v, nullptr, dout, nullptr, nullptr, dk, dv,
+                       B, H, N, d, scale, causal, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  return cuda_status(launch_bwd_main(a, stream));
+}
+
+extern "C" int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, const void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  BwdLaunch a;
+  CUtensorMap maps[4];
+  int st = prepare_bwd(a, maps, kNeedDq, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr,
+                       B, H, N, d, scale, 0, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  return cuda_status(launch_bwd_conv(a, stream));
+}
+
+extern "C" int fa_get_device_status(cudaStream_t stream) {
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  int value = 0, zero = 0;
+  if (cudaMemcpy(&value, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return value;
+}
+
+extern "C" const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK:
+      return "FA_OK";
+    case FA_ERR_INVALID_ARG:
+      return "FA_ERR_INVALID_ARG: invalid pointer, size, scale or mask flag";
+    case FA_ERR_UNSUPPORTED:
+      return "FA_ERR_UNSUPPORTED: head dimension must be 64 or 128 on an sm_103 device";
+    case FA_ERR_WORKSPACE:
+      return "FA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case FA_ERR_CUDA:
+      return "FA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case FA_ERR_DEVICE_TIMEOUT:
+      return "FA_ERR_DEVICE_TIMEOUT: a kernel gave up on a bounded wait";
+    default:
+      return "unknown fa status";
+  }
+}

@@ -1,0 +1,450 @@
+// Forward kernel: exact attention with online softmax, tcgen05 + TMA + TMEM.
+//
+// What it computes follows blog.teqners.com "13% more FLOPs, 5.7x faster ...",
+// sections "Softmax is the anti-tiling operation" (running max / normaliser)
+// and "FlashAttention's move: rescale the output, too" (rescaled output
+// accumulator, division by the normaliser after the last tile), with the loop
+// order of lensaml.com "FlashAttention" Step 3 (each CTA owns its Q rows and
+// streams K/V tiles past them, writing O once).
+//
+// Work unit: 256 query rows (two 128-row Q tiles, t = 0, 1) of one (b, h).
+// CTA roles (10 warps):
+//   warps 0-3  softmax warpgroup for Q tile 0   (thread = one query row)
+//   warps 4-7  softmax warpgroup for Q tile 1
+//   warp  8    TMA producer: Q tiles, then K_j / V_j into a STAGES-deep ring
+//   warp  9    TMEM owner and MMA issuer (one elected lane)
+// Tensor memory (512 columns): S_t at column 128 t (fp32 scores; P_t is
+// written back over its first 64 columns as packed bf16), O_t at 256 + D t.
+// Issue order on the tensor pipe alternates the two tiles:
+//   S0(j) S1(j) | PV0(j) S0(j+1) | PV1(j) S1(j+1) | PV0(j+1) ...
+// so one warpgroup's softmax overlaps the other tile's two MMAs.  Because a
+// commit covers every earlier MMA of the issuing thread, the arrival that
+// publishes S_t(j+1) also proves PV_t(j) has finished: the softmax warpgroup
+// may then rescale O_t in place before it releases P_t(j+1).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_common.cuh"
+#include "fa_kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kBlocks = D / 64;
+  static constexpr int kThreads = 320;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kColS = 0;    // + 128 t
+  static constexpr int kColO = 256;  // + D t
+  // shared memory layout (offsets from a 1024-byte aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kNumBars = 2 * 2 + 3 * kStages + 3 * 2 + 1;
+  static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
+};
+
+struct FwdBars {
+  uint64_t* q_full;    // [2]
+  uint64_t* q_empty;   // [2]
+  uint64_t* k_full;    // [S]
+  uint64_t* v_full;    // [S]
+  uint64_t* kv_empty;  // [S]
+  uint64_t* s_full;    // [2]
+  uint64_t* p_full;    // [2]
+  uint64_t* o_full;    // [2]
+  uint64_t* mma_done;  // [1]
+};
+
+// Geometry of one unit.
+struct FwdUnit {
+  int bh, q0, nq;  // slice, first query row, valid Q tiles (1 or 2)
+  int nkv[2];      // K/V tiles each Q tile visits
+  int nkv_max;
+};
+
+__device__ __forceinline__ FwdUnit fwd_decode(int pos, int nqb, int N, int nkv_total, bool causal) {
+  FwdUnit u;
+  u.bh = pos / nqb;
+  const int r = pos - u.bh * nqb;
+  const int qb = causal ? (nqb - 1 - r) : r;  // heaviest first within a slice when causal
+  u.q0 = qb * 2 * kTileRows;
+  u.nq = (u.q0 + kTileRows < N) ? 2 : 1;
+  for (int t = 0; t < 2; ++t) {
+    const int first = u.q0 + t * kTileRows;
+    if (t >= u.nq) {
+      u.nkv[t] = 0;
+    } else if (causal) {
+      const int diag = first / kTileRows;
+      u.nkv[t] = diag + 1 < nkv_total ? diag + 1 : nkv_total;
+    } else {
+      u.nkv[t] = nkv_total;
+    }
+  }
+  u.nkv_max = u.nkv[0] > u.nkv[1] ? u.nkv[0] : u.nkv[1];
+  return u;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+                  float* __restrict__ lse, int BH, int N, float c2, int* status) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+  uint8_t* sm = smem_raw + pad;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  FwdBars B;
+  B.q_full = bars;
+  B.q_empty = bars + 2;
+  B.k_full = bars + 4;
+  B.v_full = B.k_full + C::kStages;
+  B.kv_empty = B.v_full + C::kStages;
+  B.s_full = B.kv_empty + C::kStages;
+  B.p_full = B.s_full + 2;
+  B.o_full = B.p_full + 2;
+  B.mma_done = B.o_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int nqb = (N + 2 * kTileRows - 1) / (2 * kTileRows);
+  const int nkv_total = (N + kTileRows - 1) / kTileRows;
+  const int total_units = BH * nqb;
+  const int grid = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&B.q_full[t], 1);
+      mbar_init(&B.q_empty[t], 1);
+      mbar_init(&B.s_full[t], 1);
+      mbar_init(&B.p_full[t], 128);
+      mbar_init(&B.o_full[t], 1);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&B.k_full[s], 1);
+      mbar_init(&B.v_full[s], 1);
+      mbar_init(&B.kv_empty[s], 1);
+    }
+    mbar_init(B.mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      uint32_t qcnt[2] = {0, 0};
+      uint32_t kv_it = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int pos = snake_unit(round, blockIdx.x, grid);
+        if (round * grid >= total_units) break;
+        if (pos >= total_units) continue;
+        const FwdUnit u = fwd_decode(pos, nqb, N, nkv_total, CAUSAL);
+        for (int t = 0; t < u.nq && ok; ++t) {
+          ok = mbar_wait(&B.q_empty[t], (qcnt[t] & 1) ^ 1, status);
+          if (!ok) break;
+          uint8_t* dst = sm + C::kOffQ + t * C::kTileBytes;
+          mbar_expect_tx(&B.q_full[t], C::kTileBytes);
+          for (int kb = 0; kb < C::kBlocks; ++kb)
+            tma_load_3d(dst + kb * kSwzBlockBytes, &tm_q, &B.q_full[t], kb * 64, u.q0 + t * kTileRows, u.bh);
+          ++qcnt[t];
+        }
+        for (int j = 0; j < u.nkv_max && ok; ++j, ++kv_it) {
+          const int st = kv_it % C::kStages;
+          const uint32_t ph = (kv_it / C::kStages) & 1;
+          ok = mbar_wait(&B.kv_empty[st], ph ^ 1, status);
+          if (!ok) break;
+          uint8_t* kd = sm + C::kOffK + st * C::kTileBytes;
+          uint8_t* vd = sm + C::kOffV + st * C::kTileBytes;
+          mbar_expect_tx(&B.k_full[st], C::kTileBytes);
+          for (int kb = 0; kb < C::kBlocks; ++kb)
+            tma_load_3d(kd + kb * kSwzBlockBytes, &tm_k, &B.k_full[st], kb * 64, j * kTileRows, u.bh);
+          mbar_expect_tx(&B.v_full[st], C::kTileBytes);
+          for (int kb = 0; kb < C::kBlocks; ++kb)
+            tma_load_3d(vd + kb * kSwzBlockBytes, &tm_v, &B.v_full[st], kb * 64, j * kTileRows, u.bh);
+        }
+        if (aborted(abort_flag)) ok = false;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+      }
+      // Drain: every copy this warp started must have landed before exit.
+      for (int t = 0; t < 2; ++t)
+        if (qcnt[t]) mbar_wait(&B.q_full[t], (qcnt[t] - 1) & 1, status);
+      for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i) {
+        mbar_wait(&B.k_full[i % C::kStages], (i / C::kStages) & 1, status);
+        mbar_wait(&B.v_full[i % C::kStages], (i / C::kStages) & 1, status);
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0, 0);  // S = Q K^T, both K-major
+      constexpr uint32_t kIdescO = idesc_bf16(128, D, 0, 1);    // O += P V, V is MN-major
+      const uint32_t q_s = smem_addr(sm + C::kOffQ);
+      const uint32_t k_s = smem_addr(sm + C::kOffK);
+      const uint32_t v_s = smem_addr(sm + C::kOffV);
+      uint32_t qcnt[2] = {0, 0}, pcnt[2] = {0, 0};
+      uint32_t kv_it = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int pos = snake_unit(round, blockIdx.x, grid);
+        if (round * grid >= total_units) break;
+        if (pos >= total_units) continue;
+        const FwdUnit u = fwd_decode(pos, nqb, N, nkv_total, CAUSAL);
+        for (int t = 0; t < u.nq && ok; ++t) {
+          ok = mbar_wait(&B.q_full[t], qcnt[t] & 1, status);
+          ++qcnt[t];
+        }
+        if (!ok) break;
+        auto issue_s = [&](int t, int st) {
+          const uint32_t qa = q_s + t * C::kTileBytes, ka = k_s + st * C::kTileBytes;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
+            mma_ss(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdescS,
+                   k > 0);
+          }
+          mma_commit(&B.s_full[t]);
+        };
+        // prologue: S_t(0)
+        {
+          const int st = kv_it % C::kStages;
+          ok = mbar_wait(&B.k_full[st], (kv_it / C::kStages) & 1, status);
+          if (!ok) break;
+          tc_fence_after();
+          for (int t = 0; t < u.nq; ++t) issue_s(t, st);
+        }
+        for (int j = 0; j < u.nkv_max && ok; ++j) {
+          const uint32_t it = kv_it + j;
+          const int st = it % C::kStages;
+          const int st_next = (it + 1) % C::kStages;
+          bool v_ready = false, k_next_ready = false;
+          for (int t = 0; t < u.nq && ok; ++t) {
+            if (j >= u.nkv[t]) continue;
+            ok = mbar_wait(&B.p_full[t], pcnt[t] & 1, status);
+            ++pcnt[t];
+            if (!ok) break;
+            if (!v_ready) {
+              ok = mbar_wait(&B.v_full[st], (it / C::kStages) & 1, status);
+              if (!ok) break;
+              v_ready = true;
+            }
+            tc_fence_after();
+            // O_t (+)= P_t V_j : A = P_t from TMEM (8 columns per 16 keys), B = V_j MN-major
+            const uint32_t va = v_s + st * C::kTileBytes;
+#pragma unroll
+            for (int k = 0; k < kTileRows / 16; ++k)
+              mma_ts(tbase + C::kColO + D * t, tbase + C::kColS + 128 * t + k * 8,
+                     sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
+            if (j + 1 < u.nkv[t]) {
+              if (!k_next_ready) {
+                ok = mbar_wait(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                k_next_ready = true;
+              }
+              issue_s(t, st_next);
+            } else {
+              mma_commit(&B.o_full[t]);
+              mma_commit(&B.q_empty[t]);
+            }
+          }
+          if (ok) mma_commit(&B.kv_empty[st]);
+        }
+        kv_it += u.nkv_max;
+        if (aborted(abort_flag)) ok = false;
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit(B.mma_done);
+      mbar_wait(B.mma_done, 0, status);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax --
+    const int t = warp / 4;            // which Q tile this warpgroup owns
+    const int quarter = warp % 4;      // TMEM lane quarter
+    const int r = quarter * 32 + lane; // row inside the tile
+    const uint32_t t_s = tmem_lane_col(tbase, quarter * 32, C::kColS + 128 * t);
+    const uint32_t t_o = tmem_lane_col(tbase, quarter * 32, C::kColO + D * t);
+    uint32_t scnt = 0, ocnt = 0;
+    bool ok = true;
+    for (int round = 0; ok; ++round) {
+      const int pos = snake_unit(round, blockIdx.x, grid);
+      if (round * grid >= total_units) break;
+      if (pos >= total_units) continue;
+      const FwdUnit u = fwd_decode(pos, nqb, N, nkv_total, CAUSAL);
+      if (t >= u.nq) continue;
+      const int qi = u.q0 + t * kTileRows + r;  // this thread's query row
+      const int jdiag = (u.q0 + t * kTileRows) / kTileRows;
+      float m_run = -INFINITY;  // running max used by the exponentials (log2 units)
+      float l_run = 0.f;        // running normaliser relative to m_run
+      for (int j = 0; j < u.nkv[t]; ++j) {
+        ok = mbar_wait_warp(&B.s_full[t], scnt & 1, status);
+        ++scnt;
+        if (!ok) break;
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(t_s + 32 * c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(v[i]);
+        }
+        const bool tail = (j == nkv_total - 1) && (N % kTileRows != 0);
+        const bool diag = CAUSAL && (j == jdiag);
+        if (tail || diag) {
+          const int kbase = j * kTileRows;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int kj = kbase + c;
+            if (kj >= N || (CAUSAL && kj > qi)) s[c] = -INFINITY;
+          }
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float mx2 = mx * c2;  // tile max in log2 units (c2 >= 0)
+        if (j == 0) {
+          m_run = mx2;
+        } else {
+          const bool need = mx2 > m_run + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            // O_t is quiescent here (see header); rescale it and l by 2^(m_old - m_new).
+            const float m_new = fmaxf(m_run, mx2);
+            const float alpha = ex2(m_run - m_new);
+            l_run *= alpha;
+            m_run = m_new;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(t_o + 32 * c, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tmem_st32(t_o + 32 * c, v);
+            }
+          }
+        }
+        // P = 2^(s c2 - m_run), summed in fp32, stored as bf16 pairs over S_t.
+        // Masked entries are set to exactly 0 (also correct when c2 == 0).
+        float lsum = 0.f;
+        if (tail || diag) {
+          const int kbase = j * kTileRows;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int c = 64 * h + 2 * i;
+              const bool m0 = (kbase + c >= N) || (CAUSAL && kbase + c > qi);
+              const bool m1 = (kbase + c + 1 >= N) || (CAUSAL && kbase + c + 1 > qi);
+              const float p0 = m0 ? 0.f : ex2(fmaf(s[c], c2, -m_run));
+              const float p1 = m1 ? 0.f : ex2(fmaf(s[c + 1], c2, -m_run));
+              lsum += p0 + p1;
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(t_s + 32 * h, pk);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float p0 = ex2(fmaf(s[64 * h + 2 * i], c2, -m_run));
+              const float p1 = ex2(fmaf(s[64 * h + 2 * i + 1], c2, -m_run));
+              lsum += p0 + p1;
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(t_s + 32 * h, pk);
+          }
+        }
+        l_run += lsum;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&B.p_full[t]);
+      }
+      if (!ok) break;
+      // epilogue: O = O~ / l, lse = (m + log2 l) ln 2
+      ok = mbar_wait_warp(&B.o_full[t], ocnt & 1, status);
+      ++ocnt;
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = 1.f / l_run;
+      __nv_bfloat16* orow = out + ((size_t)u.bh * N + qi) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(t_o + 32 * c, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l);
+        if (qi < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (qi < N) lse[(size_t)u.bh * N + qi] = (m_run + __log2f(l_run)) * kLn2;
+      tc_fence_before();
+      if (aborted(abort_flag)) ok = false;
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, C::kTmemCols);
+  }
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v,
+                                                       reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N,
+                                                       a.c2, a.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+  return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+}
+
+int fwd_units(int BH, int N) { return BH * ((N + 2 * kTileRows - 1) / (2 * kTileRows)); }
+
+}  // namespace fa

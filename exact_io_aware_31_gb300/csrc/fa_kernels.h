@@ -1,0 +1,53 @@
+// Internal launch interface between the C ABI (fa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+
+namespace fa {
+
+struct FwdLaunch {
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  void* o;
+  float* lse;
+  int BH, N, d;
+  int causal;
+  float c2;  // scale * log2(e)
+  int* status;
+  int grid;
+};
+
+struct BwdLaunch {
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  const CUtensorMap* tm_do;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;  // [BH, N, d] fp32
+  float* lse2;    // [BH, Npad] lse * log2(e), +inf past N
+  float* dsum;    // [BH, Npad] D = rowsum(dO * O), 0 past N
+  int BH, N, Npad, d;
+  int causal;
+  float scale;
+  float c2;
+  int* status;
+  int grid;
+  int pre_grid;
+};
+
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_bwd_conv(const BwdLaunch& a, cudaStream_t stream);
+int fwd_units(int BH, int N);
+int bwd_units(int BH, int N);
+
+}  // namespace fa

@@ -1,0 +1,140 @@
+/*
+ * fa.h -- exact fused attention for NVIDIA GB300 (sm_103a): the C ABI.
+ *
+ * Computes, for every batch b and head h,
+ *
+ *     O = softmax(scale * Q K^T + mask) V
+ *
+ * tile by tile with a running row maximum and normaliser (online softmax) and
+ * a rescaled output accumulator, so the N x N score and probability matrices
+ * never reach device memory.  The forward saves O and one logsumexp per row;
+ * the backward recomputes scores and probabilities tile by tile from Q, K, V
+ * and that logsumexp.
+ *
+ * Sources (cited by page title and passage):
+ *   [T] blog.teqners.com, "13% more FLOPs, 5.7x faster: how FlashAttention's
+ *       online softmax keeps the N x N matrix out of HBM"
+ *   [L] lensaml.com, "FlashAttention" explainer
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Layout   q, k, v, o, dout, dq, dk, dv: contiguous [B, H, N, d] bf16
+ *           (row-major; element (b,h,i,c) at ((b*H + h)*N + i)*d + c).
+ *           lse: contiguous [B, H, N] fp32.
+ *  Sizes    B >= 1, H >= 1, N >= 1, d in {64, 128}; B*H*N*d < 2^31 elements
+ *           per tensor; B*H < 2^31.
+ *  scale    finite and >= 0 (typically 1/sqrt(d)); applied to Q K^T before
+ *           the mask.
+ *  causal   0: every key is visible.  1: key j is visible to query i iff
+ *           j <= i (square, top-left aligned).  No other mask is supported.
+ *  Pointers device pointers, 16-byte aligned; all memory is owned by the
+ *           caller; the library allocates no device memory on these paths.
+ *           Outputs must not overlap inputs or each other.
+ *  Streams  every call is asynchronous on `stream` (0 = legacy default);
+ *           argument validation is synchronous and leaves no CUDA error set.
+ *  Numbers  bf16 operands, fp32 accumulation and softmax; P (and dS in the
+ *           backward) rounded to bf16 before the second contraction; outputs
+ *           rounded to nearest even.  Results equal standard attention up to
+ *           rounding ([L] Step 6 and FAQ); the backward's dQ is summed with
+ *           fp32 atomics, so its last bits depend on arrival order.
+ *  Errors   a non-zero fa_status_t.  Nothing is launched when validation
+ *           fails.  A kernel that gives up waiting records
+ *           FA_ERR_DEVICE_TIMEOUT in a device status word that
+ *           fa_get_device_status() reads and clears.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size, scale, causal */
+  FA_ERR_UNSUPPORTED = 2,     /* d not in {64, 128}, or device is not sm_103 */
+  FA_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required */
+  FA_ERR_CUDA = 4,            /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up on a bounded wait */
+} fa_status_t;
+
+/*
+ * Forward pass.  [T] "FlashAttention's move: rescale the output, too";
+ * [L] Step 3 "Tiling" and Step 4 "Online Softmax".
+ *
+ *   q, k, v  in   [B, H, N, d] bf16
+ *   o        out  [B, H, N, d] bf16, O = softmax(scale * Q K^T + mask) V
+ *   lse      out  [B, H, N] fp32, natural-log logsumexp of each scaled,
+ *                 masked score row (m + ln l of the running statistics,
+ *                 [T] "The backward pass: recompute instead of read")
+ *
+ * One persistent kernel launch.  Returns FA_OK or an error above.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
+ * accumulator [B, H, N, d] and the row terms D = rowsum(dO * O) [B, H, N],
+ * each 256-byte aligned.  Returns 0 when the sizes are invalid.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass.  [T] "The backward pass: recompute instead of read": scores
+ * and probabilities are rebuilt tile by tile from q, k, v and lse; nothing of
+ * size N x N is read or written.  Gradients of L = sum(O * dO):
+ *
+ *   q, k, v, o, dout  in   [B, H, N, d] bf16 (o and lse from fa_fwd)
+ *   lse               in   [B, H, N] fp32
+ *   dq, dk, dv        out  [B, H, N, d] bf16
+ *   workspace         scratch of at least fa_bwd_workspace_size() bytes,
+ *                     256-byte aligned, owned by the caller; its contents on
+ *                     entry do not matter and are undefined on return.
+ *
+ * Three launches on `stream`: preprocess (D, zero dQ accumulator), the fused
+ * dK/dV/dQ kernel, and the dQ conversion.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
+           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The three launches of fa_bwd as separate calls, for callers that schedule
+ * or time them individually.  Running them in this order on one stream with
+ * one workspace is exactly fa_bwd; arguments mean the same as there.
+ *
+ *   fa_bwd_preprocess  reads o, dout, lse; writes the row terms
+ *                      D = rowsum(dO * O) and lse * log2(e) into the
+ *                      workspace and zeroes its fp32 dQ accumulator.
+ *   fa_bwd_dkdv        the fused recompute kernel: writes dk and dv and adds
+ *                      every dQ partial into the workspace accumulator.
+ *   fa_bwd_dq_convert  dq = scale * accumulator, rounded to bf16.
+ */
+int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv, int B, int H,
+                int N, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                cudaStream_t stream);
+int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, const void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if any kernel of this
+ * library gave up on a bounded wait since the last call; FA_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int fa_get_device_status(cudaStream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* fa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

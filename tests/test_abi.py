@@ -1,0 +1,119 @@
+"""The C-ABI library loads, exports every declared symbol and validates arguments.
+
+CPU only: nothing here reaches a device.  Every call below fails validation
+before any CUDA call, so it returns without a GPU.
+"""
+
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_io_aware_31_gb300 as fa
+from exact_io_aware_31_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(fa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(fa_[a-z_]+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "fa.h"\nint main(void){ return (int)sizeof(&fa_fwd) == 0; }\n')
+    cuda_inc = "/usr/local/cuda/include"
+    r = subprocess.run(["gcc", "-std=c99", "-fsyntax-only", "-I", os.path.dirname(HEADER), "-I", cuda_inc, str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings(lib):
+    names = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_WORKSPACE", "FA_ERR_CUDA",
+             "FA_ERR_DEVICE_TIMEOUT"]
+    for code, name in enumerate(names):
+        assert fa.fa_status_string(code).startswith(name)
+    assert fa.fa_status_string(99) == "unknown fa status"
+    assert fa.fa_status_string(-1) == "unknown fa status"
+
+
+def test_workspace_size(lib):
+    # fp32 dQ accumulator [B,H,N,d] + two fp32 row arrays [B,H,Npad], each 256-byte aligned
+    def expect(B, H, N, d):
+        r = lambda x: (x + 255) // 256 * 256
+        npad = (N + 127) // 128 * 128
+        return r(B * H * N * d * 4) + 2 * r(B * H * npad * 4)
+    for args in [(1, 2, 256, 64), (64, 16, 1024, 64), (1, 16, 16384, 128), (1, 1, 1, 128), (3, 5, 1000, 64)]:
+        assert fa.fa_bwd_workspace_size(*args) == expect(*args)
+    assert fa.fa_bwd_workspace_size(1, 1, 16, 96) == 0
+    assert fa.fa_bwd_workspace_size(0, 1, 16, 64) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 0, 64) == 0
+
+
+A = 1 << 20  # a 16-byte aligned fake address; validation fails before it is used
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), fa.FA_ERR_INVALID_ARG),
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=A + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=A + 4), fa.FA_ERR_INVALID_ARG),
+    (dict(B=1 << 16, H=1 << 16), fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_validation(lib, kw, code):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=16, d=64, scale=0.125, causal=0, stream=None)
+    args.update(kw)
+    assert fa.fa_fwd(**args) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=-5), fa.FA_ERR_INVALID_ARG),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(dout=A + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(dk=None), fa.FA_ERR_INVALID_ARG),
+    (dict(workspace=None), fa.FA_ERR_WORKSPACE),
+    (dict(workspace=A + 16), fa.FA_ERR_WORKSPACE),
+    (dict(workspace_bytes=100), fa.FA_ERR_WORKSPACE),
+])
+def test_bwd_validation(lib, kw, code):
+    args = dict(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, B=1, H=1, N=16, d=64, scale=0.125,
+                causal=1, workspace=A, workspace_bytes=1 << 30, stream=None)
+    args.update(kw)
+    assert fa.fa_bwd(**args) == code
+
+
+def test_tensor_helpers_reject_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.forward(q, q, q)
