@@ -22,7 +22,7 @@ __all__ = [
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert",
     "fa_get_device_status", "fa_status_string", "forward", "backward", "EXPORTED_SYMBOLS",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_WORKSPACE", "FA_ERR_CUDA",
-    "FA_ERR_DEVICE_TIMEOUT",
+    "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_INTERNAL",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
@@ -33,6 +33,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_WORKSPACE = 3
 FA_ERR_CUDA = 4
 FA_ERR_DEVICE_TIMEOUT = 5
+FA_ERR_INTERNAL = 6
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_dkdv",
                     "fa_bwd_dq_convert", "fa_get_device_status", "fa_status_string")

@@ -23,7 +23,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libfa.so")
 OBJDIR = os.path.join(PKG, "_build")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu"]
-HEADERS = ["fa_common.cuh", "fa_kernels.h", "sm103_ptx.cuh"]
+HEADERS = ["fa_common.cuh", "fa_kernels.h", "sm103_ptx.cuh", "exp2_poly.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
@@ -42,22 +42,31 @@ def _inputs_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def up_to_date() -> bool:
-    return os.path.exists(OUT) and os.path.getmtime(OUT) >= _inputs_mtime()
+TRACE_OUT = os.path.join(PKG, "libfa_trace.so")
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link libfa.so if any input changed; returns its path."""
-    if not force and up_to_date():
-        return OUT
-    os.makedirs(OBJDIR, exist_ok=True)
+def up_to_date(out: str = OUT) -> bool:
+    return os.path.exists(out) and os.path.getmtime(out) >= _inputs_mtime()
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=None, trace: bool = False) -> str:
+    """Compile and link libfa.so if any input changed; returns its path.
+
+    ``trace=True`` builds the phase-tracing variant ``libfa_trace.so``
+    (-DFA_TRACE) instead; the default library never contains tracing.
+    """
+    out = TRACE_OUT if trace else OUT
+    if not force and up_to_date(out):
+        return out
+    objdir = OBJDIR + ("_trace" if trace else "")
+    os.makedirs(objdir, exist_ok=True)
     exe = nvcc()
-    flags = FLAGS + list(extra_flags or [])
+    flags = FLAGS + list(extra_flags or []) + (["-DFA_TRACE"] if trace else [])
     if verbose:
         flags = flags + ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
         cmd = [exe] + ARCH + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -69,18 +78,19 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = OUT + ".tmp"
+    tmp = out + ".tmp"
     cmd = [exe] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, OUT)
-    return OUT
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true", help="print ptxas register/spill/smem usage")
+    ap.add_argument("--trace", action="store_true", help="build the phase-tracing variant libfa_trace.so")
     args = ap.parse_args()
-    print(build(force=args.force, verbose=args.verbose))
+    print(build(force=args.force, verbose=args.verbose, trace=args.trace))

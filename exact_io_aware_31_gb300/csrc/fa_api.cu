@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "fa_common.cuh"
 #include "fa_kernels.h"
 
 namespace fa {
@@ -107,6 +108,15 @@ int check_sizes(int B, int H, int N, int d, float scale, int causal) {
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// scale * log2(e), floored at 1e-30 so that a masked score (-inf) times it
+// stays -inf when scale == 0.  For finite scores |s| < 1e8 the floor changes
+// 2^(s * c2) by less than one fp32 ulp of 1, so scale == 0 still gives exact
+// uniform attention.
+float log2_scale(float scale) {
+  const float c2 = scale * 1.4426950408889634f;
+  return c2 > 1e-30f ? c2 : 1e-30f;
+}
+
 struct WorkspaceLayout {
   size_t dq_acc, lse2, dsum, total;
 };
@@ -147,7 +157,7 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   a.N = N;
   a.d = d;
   a.causal = causal;
-  a.c2 = scale * 1.4426950408889634f;
+  a.c2 = log2_scale(scale);
   a.status = dev->status;
   const int units = fwd_units(BH, N);
   a.grid = units < dev->sms ? units : dev->sms;
@@ -211,7 +221,7 @@ int prepare_bwd(BwdLaunch& a, CUtensorMap* maps, unsigned need, const void* q, c
   a.d = d;
   a.causal = causal;
   a.scale = scale;
-  a.c2 = scale * 1.4426950408889634f;
+  a.c2 = log2_scale(scale);
   a.status = dev->status;
   const int units = bwd_units(BH, N);
   a.grid = units < dev->sms ? units : dev->sms;
@@ -303,6 +313,8 @@ extern "C" const char* fa_status_string(int status) {
       return "FA_ERR_CUDA: a CUDA call or kernel launch failed";
     case FA_ERR_DEVICE_TIMEOUT:
       return "FA_ERR_DEVICE_TIMEOUT: a kernel gave up on a bounded wait";
+    case FA_ERR_INTERNAL:
+      return "FA_ERR_INTERNAL: a kernel found an internal layout assumption violated";
     default:
       return "unknown fa status";
   }

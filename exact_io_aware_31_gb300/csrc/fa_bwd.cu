@@ -11,8 +11,8 @@
 //     dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Three launches:
-//   1. fa_bwd_pre      D and log2-scaled lse per row (padded to whole tiles),
-//                      zero the fp32 dQ accumulator.            (HBM-bound)
+//   1. fa_bwd_pre      -D and -lse*log2(e) per row (padded to whole tiles with
+//                      0 and -inf), zero the fp32 dQ accumulator. (HBM-bound)
 //   2. fa_bwd_main     persistent; a unit is one 128-key tile of one (b, h);
 //                      K, V stay in shared memory while Q / dO tiles stream
 //                      past; dK, dV accumulate in TMEM; dQ partials are added
@@ -20,18 +20,23 @@
 //   3. fa_bwd_dq_conv  dQ = scale * accumulator -> bf16.       (HBM-bound)
 //
 // fa_bwd_main roles (10 warps):
-//   warps 0-3  compute warpgroup, thread = key row: P^T = 2^(S^T c2 - lse2)
-//              -> TMEM (bf16, for dV); dS^T = P^T (dP^T - D) -> shared memory
-//              (bf16, 128-byte swizzled, for dK and dQ); dK/dV epilogue
-//   warps 4-7  dQ warpgroup, thread = query row: reads each dQ partial from
-//              TMEM and reduces it into the accumulator
-//   warp  8    TMA producer
-//   warp  9    TMEM owner and MMA issuer
-// Tensor memory (512 columns): S^T [0,128) with P^T over [0,64); dP^T
-// [128,256), reused for the dQ partial once dS^T has left it; dV [256,256+d);
-// dK [256+d, 256+2d).  MMA issue order per query tile i:
-//   S^T(i) dP^T(i) | dV(i) S^T(i+1) | dK(i) dQ(i) | dP^T(i+1) ...
-// so the compute warpgroup's dS(i) overlaps dV(i) and S^T(i+1), and its
+//   warps 0-7   two compute warpgroups, thread = key row, warpgroup g owning
+//               query columns [64 g, 64 g + 64): P^T = 2^(S^T c2 - lse2) ->
+//               TMEM (bf16, over its own S^T columns, for dV);
+//               dS^T = P^T (dP^T - D) -> shared memory (bf16, 128-byte
+//               swizzled, for dK and dQ); after P of tile i they also read
+//               half of tile i-1's dQ partial from TMEM (thread = query row),
+//               release it and reduce it into the fp32 accumulator; their
+//               half of the dK/dV epilogue
+//   warp  8     TMA producer (K/V per unit, double-buffered at d = 64;
+//               Q, dO and their lse2 / D rows per query tile)
+//   warp  9     TMEM owner and MMA issuer
+// Tensor memory (512 columns): S^T [0,128) with P^T over [0,32) and
+// [64,96); dP^T [128,256); dV [256,256+d); dK [256+d, 256+2d); the dQ
+// partial in [384,448) at d = 64, and over dP^T at d = 128 (no columns left).
+// MMA issue order per query tile i:
+//   dP^T(i) | dV(i) S^T(i+1) | dK(i) dQ(i) | dP^T(i+1) ...
+// so the compute warpgroups' dS(i) overlaps dV(i) and S^T(i+1), and their
 // P(i+1) overlaps dK(i), dQ(i) and dP^T(i+1).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -86,8 +91,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restric
 #pragma unroll
     for (int off = kLanesPerRow / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (in_range && part == 0) {
-      dsum[row] = valid ? acc : 0.f;
-      lse2[row] = valid ? lse[(size_t)bh * N + i] * kLog2e : INFINITY;
+      dsum[row] = valid ? -acc : 0.f;
+      lse2[row] = valid ? -lse[(size_t)bh * N + i] * kLog2e : -INFINITY;
     }
   }
 }
@@ -110,25 +115,32 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_conv(const float* __restrict__ 
 // ------------------------------------------------------------- main kernel --
 template <int D>
 struct BwdCfg {
-  static constexpr int kStages = 2;
+  static constexpr int kStages = 2;                   // Q / dO (+ lse2 / D rows) ring
+  static constexpr int kKvStages = (D == 64) ? 2 : 1; // K / V buffers (next unit prefetch)
+  static constexpr bool kDqAliasesDp = (D == 128);    // no spare TMEM columns at d = 128
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
   static constexpr int kThreads = 320;
   static constexpr int kTmemCols = 512;
-  static constexpr int kColS = 0;
-  static constexpr int kColDP = 128;  // also the dQ partial
+  static constexpr int kColS = 0;     // S^T; P^T of query half g over columns [64 g, 64 g + 32)
+  static constexpr int kColDP = 128;  // dP^T
   static constexpr int kColDV = 256;
   static constexpr int kColDK = 256 + D;
+  static constexpr int kColDQ = kDqAliasesDp ? kColDP : 256 + 2 * D;
   static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffQ = kOffV + kTileBytes;                // [stages]
+  static constexpr int kOffV = kOffK + kKvStages * kTileBytes;
+  static constexpr int kOffQ = kOffV + kKvStages * kTileBytes;    // [stages]
   static constexpr int kOffDO = kOffQ + kStages * kTileBytes;     // [stages]
   static constexpr int kOffDS = kOffDO + kStages * kTileBytes;    // 128 x 128 bf16, two swizzle blocks
-  static constexpr int kOffBar = kOffDS + 2 * kSwzBlockBytes;
-  static constexpr int kNumBars = 2 + 3 * kStages + 11;
+  static constexpr int kOffRow = kOffDS + 2 * kSwzBlockBytes;     // [stages][lse2 128 | D 128] fp32
+  static constexpr int kRowBytes = 2 * kTileRows * 4;
+  static constexpr int kOffBar = kOffRow + kStages * kRowBytes;
+  static constexpr int kNumBars = 2 * kKvStages + 3 * kStages + 10;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
-  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
+  static constexpr int kSmemBytes = kOffAbort + 4;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kColDQ + D <= kTmemCols, "tensor memory budget");
 };
 
 struct BwdUnit {
@@ -145,6 +157,9 @@ __device__ __forceinline__ BwdUnit bwd_decode(int pos, int nkt, bool causal) {
   return u;
 }
 
+// P^T column (32-bit, bf16 pairs) holding queries 16 k .. 16 k + 15.
+__device__ __forceinline__ uint32_t pt_col(int k) { return (k < 4) ? 8 * k : 64 + 8 * (k - 4); }
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -153,14 +168,14 @@ __global__ void __launch_bounds__(320, 1)
                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int N, int Npad, float c2,
                 float scale, int* status) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
-  uint8_t* sm = smem_raw + pad;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (!smem_base_ok(smem_raw, status)) return;
+  uint8_t* sm = smem_raw;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
-  uint64_t* kv_full = bars + 0;
-  uint64_t* kv_empty = bars + 1;
-  uint64_t* q_full = bars + 2;
+  uint64_t* kv_full = bars;                       // [kv stages]
+  uint64_t* kv_empty = kv_full + C::kKvStages;    // [kv stages]
+  uint64_t* q_full = kv_empty + C::kKvStages;     // [stages]
   uint64_t* do_full = q_full + C::kStages;
   uint64_t* qdo_empty = do_full + C::kStages;
   uint64_t* s_full = qdo_empty + C::kStages;
@@ -183,22 +198,24 @@ __global__ void __launch_bounds__(320, 1)
   const int grid = gridDim.x;
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    mbar_init(kv_empty, 1);
+    for (int s = 0; s < C::kKvStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&do_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 256);
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, 256);
     mbar_init(ds_empty, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(dq_empty, 256);
     mbar_init(dkdv_full, 1);
-    mbar_init(dkdv_empty, 128);
+    mbar_init(dkdv_empty, 256);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -215,6 +232,7 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
+      Tracer tr(3);
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
@@ -226,33 +244,45 @@ __global__ void __launch_bounds__(320, 1)
         const int pos = snake_unit(round, blockIdx.x, grid);
         if (pos >= total_units) continue;
         const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
-        ok = mbar_wait(kv_empty, (ucnt & 1) ^ 1, status);
+        const int kb = ucnt % C::kKvStages;
+        tr(30);
+        ok = mbar_wait(&kv_empty[kb], ((ucnt / C::kKvStages) & 1) ^ 1, status);
+        tr(31);
         if (!ok) break;
-        mbar_expect_tx(kv_full, 2 * C::kTileBytes);
-        for (int kb = 0; kb < C::kBlocks; ++kb) {
-          tma_load_3d(sm + C::kOffK + kb * kSwzBlockBytes, &tm_k, kv_full, kb * 64, u.j * kTileRows, u.bh);
-          tma_load_3d(sm + C::kOffV + kb * kSwzBlockBytes, &tm_v, kv_full, kb * 64, u.j * kTileRows, u.bh);
+        mbar_expect_tx(&kv_full[kb], 2 * C::kTileBytes);
+        for (int b = 0; b < C::kBlocks; ++b) {
+          tma_load_3d(sm + C::kOffK + kb * C::kTileBytes + b * kSwzBlockBytes, &tm_k, &kv_full[kb], b * 64,
+                      u.j * kTileRows, u.bh);
+          tma_load_3d(sm + C::kOffV + kb * C::kTileBytes + b * kSwzBlockBytes, &tm_v, &kv_full[kb], b * 64,
+                      u.j * kTileRows, u.bh);
         }
         ++ucnt;
         for (int x = 0; x < u.nq && ok; ++x, ++it) {
           const int i = u.i0 + x;
           const int st = it % C::kStages;
+          tr(32);
           ok = mbar_wait(&qdo_empty[st], ((it / C::kStages) & 1) ^ 1, status);
+          tr(33);
           if (!ok) break;
-          mbar_expect_tx(&q_full[st], C::kTileBytes);
-          for (int kb = 0; kb < C::kBlocks; ++kb)
-            tma_load_3d(sm + C::kOffQ + st * C::kTileBytes + kb * kSwzBlockBytes, &tm_q, &q_full[st], kb * 64,
+          float* rows = reinterpret_cast<float*>(sm + C::kOffRow + st * C::kRowBytes);
+          const size_t roff = (size_t)u.bh * Npad + (size_t)i * kTileRows;
+          mbar_expect_tx(&q_full[st], C::kTileBytes + kTileRows * 4);
+          for (int b = 0; b < C::kBlocks; ++b)
+            tma_load_3d(sm + C::kOffQ + st * C::kTileBytes + b * kSwzBlockBytes, &tm_q, &q_full[st], b * 64,
                         i * kTileRows, u.bh);
-          mbar_expect_tx(&do_full[st], C::kTileBytes);
-          for (int kb = 0; kb < C::kBlocks; ++kb)
-            tma_load_3d(sm + C::kOffDO + st * C::kTileBytes + kb * kSwzBlockBytes, &tm_do, &do_full[st], kb * 64,
+          bulk_load_1d(rows, lse2 + roff, kTileRows * 4, &q_full[st]);
+          mbar_expect_tx(&do_full[st], C::kTileBytes + kTileRows * 4);
+          for (int b = 0; b < C::kBlocks; ++b)
+            tma_load_3d(sm + C::kOffDO + st * C::kTileBytes + b * kSwzBlockBytes, &tm_do, &do_full[st], b * 64,
                         i * kTileRows, u.bh);
+          bulk_load_1d(rows + kTileRows, dsum + roff, kTileRows * 4, &do_full[st]);
         }
         if (aborted(abort_flag)) ok = false;
       }
       if (!ok) *abort_flag = 1;
       // Drain copies in flight.
-      if (ucnt) mbar_wait(kv_full, (ucnt - 1) & 1, status);
+      for (uint32_t x = (ucnt > (uint32_t)C::kKvStages ? ucnt - C::kKvStages : 0); x < ucnt; ++x)
+        mbar_wait(&kv_full[x % C::kKvStages], (x / C::kKvStages) & 1, status);
       for (uint32_t x = (it > (uint32_t)C::kStages ? it - C::kStages : 0); x < it; ++x) {
         mbar_wait(&q_full[x % C::kStages], (x / C::kStages) & 1, status);
         mbar_wait(&do_full[x % C::kStages], (x / C::kStages) & 1, status);
@@ -264,28 +294,31 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T: both K-major over d
       constexpr uint32_t kIdKV = idesc_bf16(128, D, 0, 1);    // dV, dK: B (dO / Q) MN-major
       constexpr uint32_t kIdQ = idesc_bf16(128, D, 1, 1);     // dQ: A (dS) and B (K) MN-major
-      const uint32_t k_s = smem_addr(sm + C::kOffK);
-      const uint32_t v_s = smem_addr(sm + C::kOffV);
       const uint32_t q_s = smem_addr(sm + C::kOffQ);
       const uint32_t do_s = smem_addr(sm + C::kOffDO);
       const uint32_t ds_s = smem_addr(sm + C::kOffDS);
       uint32_t ucnt = 0, it = 0, pcnt = 0, dscnt = 0, dqcnt = 0;
       bool ok = true;
+      Tracer tr(2);
       auto kmajor = [](uint32_t base, int k) { return base + (k / 4) * kSwzBlockBytes + (k % 4) * 32; };
-      auto issue_st = [&](int st) {  // S^T = K Q^T
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ss(tbase + C::kColS, sdesc(kmajor(k_s, k), 16, 1024),
-                 sdesc(kmajor(q_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
-        mma_commit(s_full);
-      };
       for (int round = 0; ok; ++round) {
         if (round * grid >= total_units) break;
         const int pos = snake_unit(round, blockIdx.x, grid);
         if (pos >= total_units) continue;
         const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
-        ok = mbar_wait(kv_full, ucnt & 1, status) && mbar_wait(dkdv_empty, (ucnt & 1) ^ 1, status);
-        ++ucnt;
+        const int kb = ucnt % C::kKvStages;
+        const uint32_t k_s = smem_addr(sm + C::kOffK + kb * C::kTileBytes);
+        const uint32_t v_s = smem_addr(sm + C::kOffV + kb * C::kTileBytes);
+        auto issue_st = [&](int st) {  // S^T = K Q^T
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(tbase + C::kColS, sdesc(kmajor(k_s, k), 16, 1024),
+                   sdesc(kmajor(q_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
+          mma_commit(s_full);
+        };
+        tr(10);
+        ok = mbar_wait(&kv_full[kb], (ucnt / C::kKvStages) & 1, status);
+        tr(11);
         if (!ok) break;
         {
           const int st = it % C::kStages;
@@ -297,8 +330,10 @@ __global__ void __launch_bounds__(320, 1)
         for (int x = 0; x < u.nq && ok; ++x, ++it) {
           const int st = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
-          // dP^T(i) = V dO^T, into the columns the previous dQ partial used
-          ok = mbar_wait(&do_full[st], ph, status) && mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
+          // dP^T(i) = V dO^T
+          tr(12);
+          ok = mbar_wait(&do_full[st], ph, status);
+          if (ok && C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -306,14 +341,18 @@ __global__ void __launch_bounds__(320, 1)
             mma_ss(tbase + C::kColDP, sdesc(kmajor(v_s, k), 16, 1024),
                    sdesc(kmajor(do_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
           mma_commit(dp_full);
-          // dV += P^T dO  (A = P^T from TMEM, B = dO MN-major)
+          tr(13);
+          // dV += P^T dO  (A = P^T from TMEM, B = dO MN-major); the first of a unit
+          // also waits until the previous unit's dK/dV have been read out.
           ok = mbar_wait(p_full, pcnt & 1, status);
+          if (ok && x == 0) ok = mbar_wait(dkdv_empty, (ucnt & 1) ^ 1, status);
+          tr(14);
           ++pcnt;
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ts(tbase + C::kColDV, tbase + C::kColS + k * 8,
+            mma_ts(tbase + C::kColDV, tbase + C::kColS + pt_col(k),
                    sdesc(do_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
           // S^T(i+1) as early as possible
           if (x + 1 < u.nq) {
@@ -324,8 +363,10 @@ __global__ void __launch_bounds__(320, 1)
             issue_st(st2);
           }
           // dK += dS^T Q ; dQ_part = dS K
+          tr(15);
           ok = mbar_wait(ds_full, dscnt & 1, status);
           ++dscnt;
+          if (ok && !C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -334,34 +375,69 @@ __global__ void __launch_bounds__(320, 1)
                    sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ss(tbase + C::kColDP, sdesc(ds_s + k * 2048, kSwzBlockBytes, 1024),
+            mma_ss(tbase + C::kColDQ, sdesc(ds_s + k * 2048, kSwzBlockBytes, 1024),
                    sdesc(k_s + k * 2048, kSwzBlockBytes, 1024), kIdQ, k > 0);
           mma_commit(dq_full);
           mma_commit(ds_empty);
           mma_commit(&qdo_empty[st]);
           ++dqcnt;
+          tr(17);
         }
         if (!ok) break;
         mma_commit(dkdv_full);
-        mma_commit(kv_empty);
+        mma_commit(&kv_empty[kb]);
+        ++ucnt;
         if (aborted(abort_flag)) ok = false;
       }
       if (!ok) *abort_flag = 1;
       mma_commit(mma_done);
       mbar_wait(mma_done, 0, status);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------- compute warpgroup --
-    const int quarter = warp;
-    const int r = quarter * 32 + lane;  // key row within the tile
-    const uint32_t t_s = tmem_lane_col(tbase, quarter * 32, C::kColS);
-    const uint32_t t_dp = tmem_lane_col(tbase, quarter * 32, C::kColDP);
-    const uint32_t t_dv = tmem_lane_col(tbase, quarter * 32, C::kColDV);
-    const uint32_t t_dk = tmem_lane_col(tbase, quarter * 32, C::kColDK);
-    uint8_t* ds_row = sm + C::kOffDS + r * 128;
+  } else if (warp < 8) {
+    // ------------------------------------------------ compute warpgroups --
+    // Warpgroup g owns query columns [64 g, 64 g + 64) of P^T / dS^T and
+    // columns [g d/2, (g+1) d/2) of the dQ partial, dV and dK.
+    const int g = warp / 4;
+    const int quarter = warp % 4;
+    const int r = quarter * 32 + lane;  // key row (P, dS, dK, dV) / query row (dQ) within the tile
+    const uint32_t lanes = (uint32_t)quarter * 32;
+    const uint32_t t_s = tmem_lane_col(tbase, lanes, C::kColS + 64 * g);
+    const uint32_t t_dp = tmem_lane_col(tbase, lanes, C::kColDP + 64 * g);
+    const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + (D / 2) * g);
+    const uint32_t t_dv = tmem_lane_col(tbase, lanes, C::kColDV + (D / 2) * g);
+    const uint32_t t_dk = tmem_lane_col(tbase, lanes, C::kColDK + (D / 2) * g);
+    uint8_t* ds_row = sm + C::kOffDS + g * kSwzBlockBytes + r * 128;
     const int swz = r & 7;
-    uint32_t scnt = 0, dpcnt = 0, dse = 0, ucnt = 0;
+    const uint64_t c2x2 = f2_pack(c2, c2);
+    uint32_t scnt = 0, dpcnt = 0, dse = 0, ucnt = 0, qit = 0, dqcnt = 0;
     bool ok = true;
+    Tracer tr(warp == 0 ? 0 : -1);
+
+    // Read this warpgroup's half of dQ partial of query tile `qt` from TMEM,
+    // release the columns, then add it into the fp32 accumulator.
+    auto drain_dq = [&](int bh, int qt) -> bool {
+      tr(40);
+      if (!mbar_wait_warp(dq_full, dqcnt & 1, status)) return false;
+      ++dqcnt;
+      tc_fence_after();
+      uint32_t v[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) tmem_ld32(t_dq + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      tr(41);
+      const int q = qt * kTileRows + r;
+      if (q < N) {
+        float* dst = dq_acc + ((size_t)bh * N + q) * D + (D / 2) * g;
+#pragma unroll
+        for (int m = 0; m < D / 8; ++m)
+          red_add_v4(dst + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
+                     __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
+      }
+      return true;
+    };
+
     for (int round = 0; ok; ++round) {
       if (round * grid >= total_units) break;
       const int pos = snake_unit(round, blockIdx.x, grid);
@@ -369,106 +445,98 @@ __global__ void __launch_bounds__(320, 1)
       const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
       const int kr = u.j * kTileRows + r;  // this thread's key
       const bool key_ok = kr < N;
-      const float* l2_bh = lse2 + (size_t)u.bh * Npad;
-      const float* d_bh = dsum + (size_t)u.bh * Npad;
-      for (int x = 0; x < u.nq; ++x) {
+      for (int x = 0; x < u.nq; ++x, ++qit) {
         const int i = u.i0 + x;
-        const int q0 = i * kTileRows;
+        const int qbase = i * kTileRows + 64 * g;  // first query of this warpgroup's columns
         const bool diag = CAUSAL && (i == u.j);
-        // ---- P^T = 2^(S^T c2 - lse2), masked entries exactly 0 ----
+        // -lse2 / -D of this query tile, staged in shared memory with Q / dO
+        const float* rows =
+            reinterpret_cast<const float*>(sm + C::kOffRow + (qit % C::kStages) * C::kRowBytes) + 64 * g;
+        // ---- P^T = 2^(S^T c2 - lse2); masked entries exactly 0 ----
+        tr(1);
         ok = mbar_wait_warp(s_full, scnt & 1, status);
+        tr(2);
         ++scnt;
         if (!ok) break;
         tc_fence_after();
-        uint32_t pk[64];  // P^T row, bf16 pairs (also used for dS)
+        uint32_t pk[32];  // P^T row half, bf16 pairs (reused for dS)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t sv[32];
           tmem_ld32(t_s + 32 * c, sv);
-          float l2[32];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 v4 = __ldg(reinterpret_cast<const float4*>(l2_bh + q0 + 32 * c) + e);
-            l2[4 * e] = v4.x;
-            l2[4 * e + 1] = v4.y;
-            l2[4 * e + 2] = v4.z;
-            l2[4 * e + 3] = v4.w;
-          }
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            float p0 = ex2(fmaf(__uint_as_float(sv[2 * e]), c2, -l2[2 * e]));
-            float p1 = ex2(fmaf(__uint_as_float(sv[2 * e + 1]), c2, -l2[2 * e + 1]));
+            const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(rows + 32 * c + 2 * e);
+            const uint64_t xx = f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2x2, nl2);
+            float x0, x1;
+            f2_unpack(xx, x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
             if (diag) {
-              const int q = q0 + 32 * c + 2 * e;
+              const int q = qbase + 32 * c + 2 * e;
               if (q < kr) p0 = 0.f;
               if (q + 1 < kr) p1 = 0.f;
             }
-            if (!key_ok) {
-              p0 = 0.f;
-              p1 = 0.f;
-            }
-            pk[16 * c + e] = pack_bf16x2(p0, p1);
+            pk[16 * c + e] = key_ok ? pack_bf16x2(p0, p1) : 0u;
           }
-          uint32_t st16[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) st16[e] = pk[16 * c + e];
-          tmem_st16(t_s + 16 * c, st16);
         }
+        // S^T of this half is fully read: P^T goes over its first 32 columns.
+        tmem_st16(t_s, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(t_s + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_full);
+        tr(3);
+        // ---- dQ partial of the previous query tile ----
+        if (x > 0 && !(ok = drain_dq(u.bh, i - 1))) break;
         // ---- dS^T = P^T (dP^T - D) -> shared memory (bf16, swizzled) ----
         ok = mbar_wait_warp(dp_full, dpcnt & 1, status);
         ++dpcnt;
         if (ok) ok = mbar_wait_warp(ds_empty, (dse & 1) ^ 1, status);
         ++dse;
+        tr(4);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t dpv[32];
           tmem_ld32(t_dp + 32 * c, dpv);
-          float dd[32];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 v4 = __ldg(reinterpret_cast<const float4*>(d_bh + q0 + 32 * c) + e);
-            dd[4 * e] = v4.x;
-            dd[4 * e + 1] = v4.y;
-            dd[4 * e + 2] = v4.z;
-            dd[4 * e + 3] = v4.w;
-          }
           tmem_wait_ld();
-          uint32_t dsk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&pk[16 * c + e]);
-            const float2 pf = __bfloat1622float2(pb);
-            const float d0 = pf.x * (__uint_as_float(dpv[2 * e]) - dd[2 * e]);
-            const float d1 = pf.y * (__uint_as_float(dpv[2 * e + 1]) - dd[2 * e + 1]);
-            dsk[e] = pack_bf16x2(d0, d1);
+          for (int mm = 0; mm < 4; ++mm) {  // four 16-byte chunks = 32 queries
+            const int m = 4 * c + mm;
+            uint32_t dsk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int idx = 4 * m + e;  // pair index within the half
+              const uint64_t nd = *reinterpret_cast<const uint64_t*>(rows + kTileRows + 2 * idx);
+              const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[idx]));
+              const uint64_t t =
+                  f2_add(f2_pack(__uint_as_float(dpv[8 * mm + 2 * e]), __uint_as_float(dpv[8 * mm + 2 * e + 1])), nd);
+              float d0, d1;
+              f2_unpack(f2_mul(f2_pack(pf.x, pf.y), t), d0, d1);
+              dsk[e] = pack_bf16x2(d0, d1);
+            }
+            *reinterpret_cast<uint4*>(ds_row + ((m ^ swz) * 16)) = make_uint4(dsk[0], dsk[1], dsk[2], dsk[3]);
           }
-          // queries 32c .. 32c+31 = four 16-byte chunks in swizzle block (32c)/64
-          uint8_t* blk = ds_row + ((32 * c) / 64) * kSwzBlockBytes;
-          const int ch0 = ((32 * c) % 64) / 8;
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            *reinterpret_cast<uint4*>(blk + (((ch0 + m) ^ swz) * 16)) =
-                make_uint4(dsk[4 * m], dsk[4 * m + 1], dsk[4 * m + 2], dsk[4 * m + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(ds_full);
+        tr(5);
       }
       if (!ok) break;
-      // ---- epilogue: dV, dK (x scale) -> bf16 ----
+      // ---- dQ partial of the unit's last query tile ----
+      if (!(ok = drain_dq(u.bh, u.i0 + u.nq - 1))) break;
+      // ---- epilogue: this warpgroup's half of the dV, dK (x scale) columns -> bf16 ----
+      tr(6);
       ok = mbar_wait_warp(dkdv_full, ucnt & 1, status);
       ++ucnt;
       if (!ok) break;
       tc_fence_after();
-      const size_t rowoff = ((size_t)u.bh * N + kr) * D;
+      const size_t rowoff = ((size_t)u.bh * N + kr) * D + (D / 2) * g;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t a[32], b[32];
         tmem_ld32(t_dv + 32 * c, a);
         tmem_ld32(t_dk + 32 * c, b);
@@ -492,45 +560,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       mbar_arrive(dkdv_empty);
-      if (aborted(abort_flag)) ok = false;
-    }
-    if (!ok) *abort_flag = 1;
-  } else {
-    // ------------------------------------------------------ dQ warpgroup --
-    const int quarter = warp % 4;
-    const int r = quarter * 32 + lane;  // query row within the tile
-    const uint32_t t_dq = tmem_lane_col(tbase, quarter * 32, C::kColDP);
-    uint32_t qcnt = 0;
-    bool ok = true;
-    for (int round = 0; ok; ++round) {
-      if (round * grid >= total_units) break;
-      const int pos = snake_unit(round, blockIdx.x, grid);
-      if (pos >= total_units) continue;
-      const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
-      for (int x = 0; x < u.nq; ++x) {
-        const int q = (u.i0 + x) * kTileRows + r;
-        ok = mbar_wait_warp(dq_full, qcnt & 1, status);
-        ++qcnt;
-        if (!ok) break;
-        tc_fence_after();
-        float* dst = dq_acc + ((size_t)u.bh * N + q) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(t_dq + 32 * c, v);
-          tmem_wait_ld();
-          if (c == D / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(dq_empty);
-          }
-          if (q < N) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m)
-              red_add_v4(dst + 32 * c + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
-                         __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
-          }
-        }
-      }
+      tr(7);
       if (aborted(abort_flag)) ok = false;
     }
     if (!ok) *abort_flag = 1;
@@ -582,3 +612,8 @@ cudaError_t launch_bwd_conv(const BwdLaunch& a, cudaStream_t stream) {
 int bwd_units(int BH, int N) { return BH * ((N + kTileRows - 1) / kTileRows); }
 
 }  // namespace fa
+
+#ifdef FA_TRACE
+// Trace builds only: phase records of this file's kernels.
+extern "C" int fa_trace_dump_bwd(void* host, size_t bytes) { return fa::trace_dump(host, bytes); }
+#endif

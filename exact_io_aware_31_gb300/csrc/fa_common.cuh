@@ -1,7 +1,11 @@
 // Shared constants and the persistent schedule of the attention kernels.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
+#ifdef FA_TRACE
+#include <cuda_runtime.h>
+#endif
 
 namespace fa {
 
@@ -25,6 +29,52 @@ __host__ __device__ inline int snake_unit(int round, int cta, int grid) {
 }
 
 #ifdef __CUDACC__
+// Phase tracing, compiled in only with -DFA_TRACE (a separate build of the
+// library, never the default one).  Lane 0 of a traced role appends
+// (clock64 << 8 | tag) records for the first kTraceCtas CTAs into this
+// translation unit's device buffer, which its fa_trace_dump_<unit>() copies
+// out.  Without FA_TRACE a Tracer is an empty object and every call compiles
+// away.
+constexpr int kTraceCtas = 4;
+constexpr int kTraceRoles = 4;
+constexpr int kTraceCap = 8192;
+#ifdef FA_TRACE
+static __device__ unsigned long long g_fa_trace[kTraceCtas * kTraceRoles * kTraceCap];
+
+// Copy (and clear) this translation unit's trace buffer; trace builds only.
+static inline int trace_dump(void* host, size_t bytes) {
+  const size_t n = sizeof(unsigned long long) * kTraceCtas * kTraceRoles * kTraceCap;
+  if (host == nullptr || bytes < n) return 1;
+  if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpyFromSymbol(host, g_fa_trace, n) != cudaSuccess) {
+    cudaGetLastError();
+    return 4;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fa_trace) != cudaSuccess || cudaMemset(p, 0, n) != cudaSuccess) {
+    cudaGetLastError();
+    return 4;
+  }
+  return 0;
+}
+struct Tracer {
+  unsigned long long* p;
+  int n;
+  __device__ explicit Tracer(int role)  // role < 0: not traced
+      : p((blockIdx.x < kTraceCtas && role >= 0) ? g_fa_trace + (blockIdx.x * kTraceRoles + role) * kTraceCap
+                                                  : nullptr),
+        n(0) {}
+  __device__ __forceinline__ void operator()(int tag) {
+    if (p != nullptr && (threadIdx.x & 31) == 0 && n < kTraceCap)
+      p[n++] = (static_cast<unsigned long long>(clock64()) << 8) | static_cast<unsigned>(tag & 0xff);
+  }
+};
+#else
+struct Tracer {
+  __device__ explicit Tracer(int) {}
+  __device__ __forceinline__ void operator()(int) {}
+};
+#endif
+
 // CTA-local abort flag: set by a role that gave up on a bounded wait, polled
 // by the others between units so the whole CTA leaves promptly.
 __device__ __forceinline__ bool aborted(const volatile int* flag) { return *flag != 0; }

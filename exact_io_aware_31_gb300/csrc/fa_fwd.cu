@@ -34,6 +34,7 @@ namespace fa {
 template <int D>
 struct FwdCfg {
   static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kQBufs = (D == 128) ? 1 : 2;  // Q buffers per tile (next unit's Q prefetched at d = 64)
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
   static constexpr int kThreads = 320;
@@ -42,18 +43,18 @@ struct FwdCfg {
   static constexpr int kColO = 256;  // + D t
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffK = kOffQ + 2 * kQBufs * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  static constexpr int kNumBars = 2 * 2 + 3 * kStages + 3 * 2 + 1;
+  static constexpr int kNumBars = 2 * 2 * kQBufs + 3 * kStages + 3 * 2 + 1;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
-  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffAbort + 4;
 };
 
 struct FwdBars {
-  uint64_t* q_full;    // [2]
-  uint64_t* q_empty;   // [2]
+  uint64_t* q_full;    // [2][kQBufs]
+  uint64_t* q_empty;   // [2][kQBufs]
   uint64_t* k_full;    // [S]
   uint64_t* v_full;    // [S]
   uint64_t* kv_empty;  // [S]
@@ -65,9 +66,10 @@ struct FwdBars {
 
 // Geometry of one unit.
 struct FwdUnit {
-  int bh, q0, nq;  // slice, first query row, valid Q tiles (1 or 2)
-  int nkv[2];      // K/V tiles each Q tile visits
+  int bh, q0, nq;    // slice, first query row, valid Q tiles (1 or 2)
+  int nkv0, nkv1;    // K/V tiles Q tile 0 / 1 visits
   int nkv_max;
+  __device__ __forceinline__ int nkv(int t) const { return t ? nkv1 : nkv0; }
 };
 
 __device__ __forceinline__ FwdUnit fwd_decode(int pos, int nqb, int N, int nkv_total, bool causal) {
@@ -77,18 +79,22 @@ __device__ __forceinline__ FwdUnit fwd_decode(int pos, int nqb, int N, int nkv_t
   const int qb = causal ? (nqb - 1 - r) : r;  // heaviest first within a slice when causal
   u.q0 = qb * 2 * kTileRows;
   u.nq = (u.q0 + kTileRows < N) ? 2 : 1;
+  int n[2];
+#pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int first = u.q0 + t * kTileRows;
     if (t >= u.nq) {
-      u.nkv[t] = 0;
+      n[t] = 0;
     } else if (causal) {
       const int diag = first / kTileRows;
-      u.nkv[t] = diag + 1 < nkv_total ? diag + 1 : nkv_total;
+      n[t] = diag + 1 < nkv_total ? diag + 1 : nkv_total;
     } else {
-      u.nkv[t] = nkv_total;
+      n[t] = nkv_total;
     }
   }
-  u.nkv_max = u.nkv[0] > u.nkv[1] ? u.nkv[0] : u.nkv[1];
+  u.nkv0 = n[0];
+  u.nkv1 = n[1];
+  u.nkv_max = n[0] > n[1] ? n[0] : n[1];
   return u;
 }
 
@@ -98,15 +104,15 @@ __global__ void __launch_bounds__(320, 1)
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ lse, int BH, int N, float c2, int* status) {
   using C = FwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
-  uint8_t* sm = smem_raw + pad;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (!smem_base_ok(smem_raw, status)) return;
+  uint8_t* sm = smem_raw;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   FwdBars B;
   B.q_full = bars;
-  B.q_empty = bars + 2;
-  B.k_full = bars + 4;
+  B.q_empty = bars + 2 * C::kQBufs;
+  B.k_full = bars + 4 * C::kQBufs;
   B.v_full = B.k_full + C::kStages;
   B.kv_empty = B.v_full + C::kStages;
   B.s_full = B.kv_empty + C::kStages;
@@ -124,9 +130,11 @@ __global__ void __launch_bounds__(320, 1)
   const int grid = gridDim.x;
 
   if (threadIdx.x == 0) {
+    for (int q = 0; q < 2 * C::kQBufs; ++q) {
+      mbar_init(&B.q_full[q], 1);
+      mbar_init(&B.q_empty[q], 1);
+    }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&B.q_full[t], 1);
-      mbar_init(&B.q_empty[t], 1);
       mbar_init(&B.s_full[t], 1);
       mbar_init(&B.p_full[t], 128);
       mbar_init(&B.o_full[t], 1);
@@ -152,6 +160,7 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
+      Tracer tr(3);
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
@@ -163,19 +172,26 @@ __global__ void __launch_bounds__(320, 1)
         if (round * grid >= total_units) break;
         if (pos >= total_units) continue;
         const FwdUnit u = fwd_decode(pos, nqb, N, nkv_total, CAUSAL);
-        for (int t = 0; t < u.nq && ok; ++t) {
-          ok = mbar_wait(&B.q_empty[t], (qcnt[t] & 1) ^ 1, status);
+        tr(30);
+        #pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= u.nq || !ok) continue;
+          const int qb = t * C::kQBufs + qcnt[t] % C::kQBufs;
+          ok = mbar_wait(&B.q_empty[qb], ((qcnt[t] / C::kQBufs) & 1) ^ 1, status);
+          tr(31);
           if (!ok) break;
-          uint8_t* dst = sm + C::kOffQ + t * C::kTileBytes;
-          mbar_expect_tx(&B.q_full[t], C::kTileBytes);
+          uint8_t* dst = sm + C::kOffQ + qb * C::kTileBytes;
+          mbar_expect_tx(&B.q_full[qb], C::kTileBytes);
           for (int kb = 0; kb < C::kBlocks; ++kb)
-            tma_load_3d(dst + kb * kSwzBlockBytes, &tm_q, &B.q_full[t], kb * 64, u.q0 + t * kTileRows, u.bh);
+            tma_load_3d(dst + kb * kSwzBlockBytes, &tm_q, &B.q_full[qb], kb * 64, u.q0 + t * kTileRows, u.bh);
           ++qcnt[t];
         }
         for (int j = 0; j < u.nkv_max && ok; ++j, ++kv_it) {
           const int st = kv_it % C::kStages;
           const uint32_t ph = (kv_it / C::kStages) & 1;
+          tr(32);
           ok = mbar_wait(&B.kv_empty[st], ph ^ 1, status);
+          tr(33);
           if (!ok) break;
           uint8_t* kd = sm + C::kOffK + st * C::kTileBytes;
           uint8_t* vd = sm + C::kOffV + st * C::kTileBytes;
@@ -192,8 +208,10 @@ __global__ void __launch_bounds__(320, 1)
         *abort_flag = 1;
       }
       // Drain: every copy this warp started must have landed before exit.
+#pragma unroll
       for (int t = 0; t < 2; ++t)
-        if (qcnt[t]) mbar_wait(&B.q_full[t], (qcnt[t] - 1) & 1, status);
+        for (uint32_t x = (qcnt[t] > (uint32_t)C::kQBufs ? qcnt[t] - C::kQBufs : 0); x < qcnt[t]; ++x)
+          mbar_wait(&B.q_full[t * C::kQBufs + x % C::kQBufs], (x / C::kQBufs) & 1, status);
       for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i) {
         mbar_wait(&B.k_full[i % C::kStages], (i / C::kStages) & 1, status);
         mbar_wait(&B.v_full[i % C::kStages], (i / C::kStages) & 1, status);
@@ -210,18 +228,25 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t qcnt[2] = {0, 0}, pcnt[2] = {0, 0};
       uint32_t kv_it = 0;
       bool ok = true;
+      Tracer tr(2);
       for (int round = 0; ok; ++round) {
         const int pos = snake_unit(round, blockIdx.x, grid);
         if (round * grid >= total_units) break;
         if (pos >= total_units) continue;
         const FwdUnit u = fwd_decode(pos, nqb, N, nkv_total, CAUSAL);
-        for (int t = 0; t < u.nq && ok; ++t) {
-          ok = mbar_wait(&B.q_full[t], qcnt[t] & 1, status);
+        tr(10);
+        int qbuf[2] = {0, 0};  // Q buffer (t * kQBufs + b) each tile uses in this unit
+        #pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= u.nq || !ok) continue;
+          qbuf[t] = t * C::kQBufs + qcnt[t] % C::kQBufs;
+          ok = mbar_wait(&B.q_full[qbuf[t]], (qcnt[t] / C::kQBufs) & 1, status);
           ++qcnt[t];
         }
+        tr(11);
         if (!ok) break;
         auto issue_s = [&](int t, int st) {
-          const uint32_t qa = q_s + t * C::kTileBytes, ka = k_s + st * C::kTileBytes;
+          const uint32_t qa = q_s + qbuf[t] * C::kTileBytes, ka = k_s + st * C::kTileBytes;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
@@ -236,16 +261,24 @@ __global__ void __launch_bounds__(320, 1)
           ok = mbar_wait(&B.k_full[st], (kv_it / C::kStages) & 1, status);
           if (!ok) break;
           tc_fence_after();
-          for (int t = 0; t < u.nq; ++t) issue_s(t, st);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t < u.nq) issue_s(t, st);
+            if (t < u.nq && u.nkv(t) == 1) mma_commit(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+          }
         }
         for (int j = 0; j < u.nkv_max && ok; ++j) {
           const uint32_t it = kv_it + j;
           const int st = it % C::kStages;
           const int st_next = (it + 1) % C::kStages;
           bool v_ready = false, k_next_ready = false;
-          for (int t = 0; t < u.nq && ok; ++t) {
-            if (j >= u.nkv[t]) continue;
+          #pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= u.nq || !ok) continue;
+            if (j >= u.nkv(t)) continue;
+            tr(20 + t);
             ok = mbar_wait(&B.p_full[t], pcnt[t] & 1, status);
+            tr(22 + t);
             ++pcnt[t];
             if (!ok) break;
             if (!v_ready) {
@@ -260,7 +293,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int k = 0; k < kTileRows / 16; ++k)
               mma_ts(tbase + C::kColO + D * t, tbase + C::kColS + 128 * t + k * 8,
                      sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
-            if (j + 1 < u.nkv[t]) {
+            if (j + 1 < u.nkv(t)) {
               if (!k_next_ready) {
                 ok = mbar_wait(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
                 if (!ok) break;
@@ -268,10 +301,11 @@ __global__ void __launch_bounds__(320, 1)
                 k_next_ready = true;
               }
               issue_s(t, st_next);
+              if (j + 2 == u.nkv(t)) mma_commit(&B.q_empty[qbuf[t]]);  // last S_t of the unit
             } else {
               mma_commit(&B.o_full[t]);
-              mma_commit(&B.q_empty[t]);
             }
+            tr(24 + t);
           }
           if (ok) mma_commit(&B.kv_empty[st]);
         }
@@ -291,6 +325,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t t_o = tmem_lane_col(tbase, quarter * 32, C::kColO + D * t);
     uint32_t scnt = 0, ocnt = 0;
     bool ok = true;
+    Tracer tr(quarter == 0 ? t : -1);
     for (int round = 0; ok; ++round) {
       const int pos = snake_unit(round, blockIdx.x, grid);
       if (round * grid >= total_units) break;
@@ -301,34 +336,41 @@ __global__ void __launch_bounds__(320, 1)
       const int jdiag = (u.q0 + t * kTileRows) / kTileRows;
       float m_run = -INFINITY;  // running max used by the exponentials (log2 units)
       float l_run = 0.f;        // running normaliser relative to m_run
-      for (int j = 0; j < u.nkv[t]; ++j) {
+      for (int j = 0; j < u.nkv(t); ++j) {
+        tr(1);
         ok = mbar_wait_warp(&B.s_full[t], scnt & 1, status);
+        tr(2);
         ++scnt;
         if (!ok) break;
         tc_fence_after();
-        float s[128];
+        // Whole S row into registers: four loads in flight, one wait.
+        uint32_t sv[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(t_s + 32 * c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(v[i]);
+          uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]);
+          tmem_ld32(t_s + 32 * c, chunk);
         }
+        tmem_wait_ld();
+        tr(3);
+        float* s = reinterpret_cast<float*>(sv);
         const bool tail = (j == nkv_total - 1) && (N % kTileRows != 0);
         const bool diag = CAUSAL && (j == jdiag);
         if (tail || diag) {
+          // Masked keys -> -inf: key kbase + c is visible iff c <= cut.
           const int kbase = j * kTileRows;
+          const int lim = CAUSAL ? min(qi, N - 1) : N - 1;
+          const int cut = lim - kbase;
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int kj = kbase + c;
-            if (kj >= N || (CAUSAL && kj > qi)) s[c] = -INFINITY;
-          }
+          for (int c = 0; c < 128; ++c) s[c] = (c > cut) ? -INFINITY : s[c];
         }
-        float mx = s[0];
+        // Row max: three-input max, eight independent partial maxima.
+        float pm[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        const float mx2 = mx * c2;  // tile max in log2 units (c2 >= 0)
+        for (int e = 0; e < 8; ++e) pm[e] = max3f(s[2 * e], s[2 * e + 1], -INFINITY);
+#pragma unroll
+        for (int c = 16; c < 128; c += 2) pm[(c / 2) & 7] = max3f(pm[(c / 2) & 7], s[c], s[c + 1]);
+        const float mx = max3f(max3f(pm[0], pm[1], pm[2]), max3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+        const float mx2 = mx * c2;  // tile max in log2 units (c2 > 0)
         if (j == 0) {
           m_run = mx2;
         } else {
@@ -339,59 +381,70 @@ __global__ void __launch_bounds__(320, 1)
             const float alpha = ex2(m_run - m_new);
             l_run *= alpha;
             m_run = m_new;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t v[32];
-              tmem_ld32(t_o + 32 * c, v);
+            const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t v[16];
+              tmem_ld16(t_o + 16 * c, v);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(t_o + 32 * c, v);
+              for (int i = 0; i < 8; ++i) {
+                float lo, hi;
+                f2_unpack(f2_mul(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), a2), lo, hi);
+                v[2 * i] = __float_as_uint(lo);
+                v[2 * i + 1] = __float_as_uint(hi);
+              }
+              tmem_st16(t_o + 16 * c, v);
             }
           }
         }
-        // P = 2^(s c2 - m_run), summed in fp32, stored as bf16 pairs over S_t.
-        // Masked entries are set to exactly 0 (also correct when c2 == 0).
-        float lsum = 0.f;
-        if (tail || diag) {
-          const int kbase = j * kTileRows;
+        tr(4);
+        // P = 2^(s c2 - m_run) in pairs, summed in fp32, stored as bf16 pairs over
+        // S_t in four 16-column pieces.  One pair in four takes the FMA-pipe
+        // polynomial instead of MUFU (unmasked tiles only, so masked entries
+        // stay exactly 0).
+        const uint64_t c2x2 = f2_pack(c2, c2);
+        const uint64_t negm = f2_pack(-m_run, -m_run);
+        const bool use_poly = !(tail || diag);
+        uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};  // partial row sums (pairs)
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t pk[32];
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int c = 64 * h + 2 * i;
-              const bool m0 = (kbase + c >= N) || (CAUSAL && kbase + c > qi);
-              const bool m1 = (kbase + c + 1 >= N) || (CAUSAL && kbase + c + 1 > qi);
-              const float p0 = m0 ? 0.f : ex2(fmaf(s[c], c2, -m_run));
-              const float p1 = m1 ? 0.f : ex2(fmaf(s[c + 1], c2, -m_run));
-              lsum += p0 + p1;
-              pk[i] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < 16; ++i) {
+            const int c = 32 * h + 2 * i;
+            const uint64_t x = f2_fma(f2_pack(s[c], s[c + 1]), c2x2, negm);
+            uint64_t p;
+            if (use_poly && (i & 3) == 3) {
+              p = ex2_poly2(x);
+            } else {
+              float x0, x1;
+              f2_unpack(x, x0, x1);
+              p = f2_pack(ex2(x0), ex2(x1));
             }
-            tmem_st32(t_s + 32 * h, pk);
+            ls[i & 3] = f2_add(ls[i & 3], p);
+            float p0, p1;
+            f2_unpack(p, p0, p1);
+            pk[i] = pack_bf16x2(p0, p1);
           }
-        } else {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float p0 = ex2(fmaf(s[64 * h + 2 * i], c2, -m_run));
-              const float p1 = ex2(fmaf(s[64 * h + 2 * i + 1], c2, -m_run));
-              lsum += p0 + p1;
-              pk[i] = pack_bf16x2(p0, p1);
-            }
-            tmem_st32(t_s + 32 * h, pk);
-          }
+          tmem_st16(t_s + 16 * h, pk);
         }
-        l_run += lsum;
+        {
+          const uint64_t t01 = f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3]));
+          float a0, a1;
+          f2_unpack(t01, a0, a1);
+          l_run += a0 + a1;
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&B.p_full[t]);
+        tr(5);
       }
       if (!ok) break;
       // epilogue: O = O~ / l, lse = (m + log2 l) ln 2
+      tr(6);
       ok = mbar_wait_warp(&B.o_full[t], ocnt & 1, status);
+      tr(7);
       ++ocnt;
       if (!ok) break;
       tc_fence_after();
@@ -413,6 +466,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       if (qi < N) lse[(size_t)u.bh * N + qi] = (m_run + __log2f(l_run)) * kLn2;
+      tr(8);
       tc_fence_before();
       if (aborted(abort_flag)) ok = false;
     }
@@ -448,3 +502,8 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
 int fwd_units(int BH, int N) { return BH * ((N + 2 * kTileRows - 1) / (2 * kTileRows)); }
 
 }  // namespace fa
+
+#ifdef FA_TRACE
+// Trace builds only: phase records of this file's kernels.
+extern "C" int fa_trace_dump_fwd(void* host, size_t bytes) { return fa::trace_dump(host, bytes); }
+#endif

@@ -9,14 +9,27 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "exp2_poly.h"
+
 namespace fa {
 
 // ---------------------------------------------------------------- errors ----
 // Device status codes written into the library's status word (see fa.h).
 enum : int {
   kDevOk = 0,
-  kDevTimeout = 5,  // FA_ERR_DEVICE_TIMEOUT
+  kDevTimeout = 5,   // FA_ERR_DEVICE_TIMEOUT
+  kDevInternal = 6,  // FA_ERR_INTERNAL
 };
+
+// Shared-memory tiles are laid out from the dynamic shared memory base, which
+// must be 1024-byte aligned for the 128-byte swizzle atoms.  On sm_103 the
+// base follows the 1 KiB reserved block and is 1024-aligned; a kernel that
+// finds otherwise records kDevInternal and returns before touching memory.
+__device__ __forceinline__ bool smem_base_ok(const void* base, int* status) {
+  if ((static_cast<uint32_t>(__cvta_generic_to_shared(base)) & 1023u) == 0) return true;
+  if (threadIdx.x == 0) atomicExch(status, kDevInternal);
+  return false;
+}
 
 // Every mbarrier wait gives up after this many nanoseconds of global time,
 // records kDevTimeout and lets the CTA leave cleanly.  Legitimate waits in
@@ -120,6 +133,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple
+// of 16), completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -279,6 +302,60 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Paired fp32 arithmetic (two lanes of a 64-bit register pair per instruction).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x on the FMA pipe for a pair of arguments, x <= 126 (see exp2_poly.h):
+// j = round(x) through the 1.5 * 2^23 shift, f = x - j in [-1/2, 1/2],
+// p(f) ~ 2^f (relative error < 7.5e-5), then j added to p's exponent field.
+// Arguments below -125 are clamped there (result ~2^-125 instead of ~0).
+__device__ __forceinline__ uint64_t ex2_poly2(uint64_t x) {
+  float x0, x1;
+  f2_unpack(x, x0, x1);
+  x0 = fmaxf(x0, -125.f);
+  x1 = fmaxf(x1, -125.f);
+  const uint64_t shift = f2_pack(12582912.f, 12582912.f);
+  const uint64_t xc = f2_pack(x0, x1);
+  const uint64_t t = f2_add(xc, shift);
+  const uint64_t j = f2_add(t, f2_pack(-12582912.f, -12582912.f));
+  const uint64_t f = f2_fma(j, f2_pack(-1.f, -1.f), xc);  // x - j
+  uint64_t p = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
+  p = f2_fma(p, f, f2_pack(kExp2C1, kExp2C1));
+  p = f2_fma(p, f, f2_pack(kExp2C0, kExp2C0));
+  float p0, p1, t0, t1;
+  f2_unpack(p, p0, p1);
+  f2_unpack(t, t0, t1);
+  return f2_pack(__int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23)),
+                 __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23)));
 }
 
 // Pack two floats to bf16x2 (round to nearest even): `lo` in bits 0..15.

@@ -39,7 +39,8 @@
  *           fp32 atomics, so its last bits depend on arrival order.
  *  Errors   a non-zero fa_status_t.  Nothing is launched when validation
  *           fails.  A kernel that gives up waiting records
- *           FA_ERR_DEVICE_TIMEOUT in a device status word that
+ *           FA_ERR_DEVICE_TIMEOUT (FA_ERR_INTERNAL if it finds its shared
+ *           memory misaligned) in a device status word that
  *           fa_get_device_status() reads and clears.
  */
 #ifndef FA_H_
@@ -58,7 +59,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,     /* d not in {64, 128}, or device is not sm_103 */
   FA_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required */
   FA_ERR_CUDA = 4,            /* a CUDA runtime/driver call or launch failed */
-  FA_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up on a bounded wait */
+  FA_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up on a bounded wait */
+  FA_ERR_INTERNAL = 6         /* a kernel found an internal layout assumption violated */
 } fa_status_t;
 
 /*
@@ -125,7 +127,8 @@ int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, const v
 /*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if any kernel of this
- * library gave up on a bounded wait since the last call; FA_ERR_CUDA if the
+ * library gave up on a bounded wait since the last call (FA_ERR_INTERNAL for
+ * a violated layout assumption); FA_ERR_CUDA if the
  * synchronisation itself failed.
  */
 int fa_get_device_status(cudaStream_t stream);

@@ -52,7 +52,7 @@ def test_header_compiles_as_c(tmp_path):
 
 def test_status_strings(lib):
     names = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_WORKSPACE", "FA_ERR_CUDA",
-             "FA_ERR_DEVICE_TIMEOUT"]
+             "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_INTERNAL"]
     for code, name in enumerate(names):
         assert fa.fa_status_string(code).startswith(name)
     assert fa.fa_status_string(99) == "unknown fa status"

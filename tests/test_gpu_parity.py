@@ -5,7 +5,10 @@
   dims, both masks, batched heads.
 * Stress inputs: queries x8 (score rows spanning dozens of units, so the
   running maximum moves and the lazy rescale fires), one spiked key per head,
-  sorted keys (the maximum keeps growing along the row).
+  sorted keys (the maximum keeps growing along the row).  Their rows are
+  dominated by single keys, so the bounds add the bf16 effects that then
+  surface: one ulp of |O| on the output, and the first-order effect of D being
+  formed from the stored bf16 O on dQ and dK (tests/gpu_util.py).
 * scale = 0 (uniform attention, closed form).
 """
 
@@ -15,7 +18,8 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.gpu_util import (assert_fwd_close, assert_grads_close, require_gpu, run_bwd, run_fwd)
+from tests.gpu_util import (assert_fwd_close, assert_grads_close, d_rounding_allowance, require_gpu, run_bwd,
+                            run_fwd)
 from workloads import make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -62,8 +66,10 @@ def test_stress_inputs(stress, N, d, causal):
     qg, kg, vg, o, lse = run_fwd(q, k, v, scale, causal)
     grads = run_bwd(qg, kg, vg, o, lse, do, scale, causal)
     o_ref, lse_ref, g_ref = _oracle_case(q, k, v, do, scale, causal)
-    assert_fwd_close(o, lse, o_ref, lse_ref, stress)
-    assert_grads_close(grads, g_ref, stress)
+    assert_fwd_close(o, lse, o_ref, lse_ref, stress, o_rel=2.0 ** -8)
+    extra = d_rounding_allowance(q.double().numpy(), k.double().numpy(), do.double().numpy(), o_ref, lse_ref,
+                                 scale, causal)
+    assert_grads_close(grads, g_ref, stress, extra=extra)
 
 
 @pytest.mark.parametrize("causal", [False, True])
