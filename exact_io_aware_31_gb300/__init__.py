@@ -19,7 +19,7 @@ import os
 
 __all__ = [
     "LIB_PATH", "FaError", "load_library", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
-    "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert",
+    "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "fa_get_device_status", "fa_status_string", "forward", "backward", "EXPORTED_SYMBOLS",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_WORKSPACE", "FA_ERR_CUDA",
     "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_INTERNAL",
@@ -36,7 +36,10 @@ FA_ERR_DEVICE_TIMEOUT = 5
 FA_ERR_INTERNAL = 6
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_dkdv",
-                    "fa_bwd_dq_convert", "fa_get_device_status", "fa_status_string")
+                    "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_get_device_status", "fa_status_string")
+
+# Size of the library-owned scratch behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
 
@@ -70,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_bwd_dq_convert.restype = i
     lib.fa_bwd_dq_convert.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
+    lib.fa_bwd_noalloc.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_get_device_status.restype = i
     lib.fa_get_device_status.argtypes = [vp]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -104,6 +109,11 @@ def fa_bwd_dkdv(q, k, v, dout, dk, dv, B, H, N, d, scale, causal, workspace, wor
 
 def fa_bwd_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream) -> int:
     return load_library().fa_bwd_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, stream) -> int:
+    """fa_bwd with the library's own scratch instead of a workspace (for callers that cannot allocate)."""
+    return load_library().fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, stream)
 
 
 def fa_get_device_status(stream) -> int:

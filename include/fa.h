@@ -125,6 +125,36 @@ int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, const v
                       size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Size of the library-owned scratch fa_bwd_noalloc uses: 64 MiB, held on every
+ * GPU that loads the library until the process exits.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * Backward pass without a caller-supplied workspace.  The pages have no
+ * counterpart: this serves callers that cannot allocate device memory (code
+ * running where cudaMalloc is forbidden or unwanted, such as inside an
+ * allocator hook or a plug-in that must not touch the process's memory pool).
+ * Arguments and results are those of fa_bwd; the workspace is a file-scope
+ * device array of FA_NOALLOC_SCRATCH_BYTES owned by the library, and nothing
+ * is allocated or freed by the call.
+ *
+ *   Limit     fa_bwd_workspace_size(B, H, N, d) must not exceed
+ *             FA_NOALLOC_SCRATCH_BYTES; larger sizes return FA_ERR_WORKSPACE
+ *             without launching anything (e.g. B*H*N*d up to ~16M elements).
+ *   Set-up    the first call on each device looks up the scratch's device
+ *             address (cudaGetSymbolAddress) with that device current; make
+ *             that first call before any stream capture.
+ *   Sharing   every call on a device uses the same scratch, which keeps the
+ *             last call's contents (the call itself clears what must start at
+ *             zero).  Calls that overlap on the GPU (different streams, no
+ *             ordering between them) race on it and give wrong results.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                   int causal, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if any kernel of this
  * library gave up on a bounded wait since the last call (FA_ERR_INTERNAL for
