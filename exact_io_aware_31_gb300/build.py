@@ -49,16 +49,18 @@ def up_to_date(out: str = OUT) -> bool:
     return os.path.exists(out) and os.path.getmtime(out) >= _inputs_mtime()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None, trace: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=None, trace: bool = False, out: str = None) -> str:
     """Compile and link libfa.so if any input changed; returns its path.
 
     ``trace=True`` builds the phase-tracing variant ``libfa_trace.so``
     (-DFA_TRACE) instead; the default library never contains tracing.
+    ``out`` (with ``extra_flags``) builds a tuning variant at another path.
     """
-    out = TRACE_OUT if trace else OUT
-    if not force and up_to_date(out):
+    custom = out is not None
+    out = out or (TRACE_OUT if trace else OUT)
+    if not force and not custom and up_to_date(out):
         return out
-    objdir = OBJDIR + ("_trace" if trace else "")
+    objdir = (out + ".objs") if custom else OBJDIR + ("_trace" if trace else "")
     os.makedirs(objdir, exist_ok=True)
     exe = nvcc()
     flags = FLAGS + list(extra_flags or []) + (["-DFA_TRACE"] if trace else [])

@@ -92,6 +92,19 @@ int make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// [B*H, N, d] fp32 (the dQ accumulator): 128-row x 32-column boxes,
+// 128-byte swizzle, used by the tensor reduce-add of the d = 64 backward.
+int make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_sizes(int B, int H, int N, int d, float scale, int causal) {
@@ -202,6 +215,8 @@ int prepare_bwd(BwdLaunch& a, CUtensorMap* maps, unsigned need, const void* q, c
       return FA_ERR_CUDA;
   }
   uint8_t* ws = static_cast<uint8_t*>(const_cast<void*>(workspace));
+  if ((need & kNeedQKV) && make_map_f32(&maps[4], ws + w.dq_acc, BH, N, d)) return FA_ERR_CUDA;
+  a.tm_dqacc = &maps[4];
   a.tm_q = &maps[0];
   a.tm_k = &maps[1];
   a.tm_v = &maps[2];
@@ -242,7 +257,7 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
                       void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   BwdLaunch a;
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   int st = prepare_bwd(a, maps, kNeedQKV | kNeedO | kNeedDout | kNeedLse | kNeedDq | kNeedDkDv, q, k, v, o, dout,
                        lse, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes);
   if (st != FA_OK) return st;
@@ -254,7 +269,7 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
 extern "C" int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   BwdLaunch a;
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   int st = prepare_bwd(a, maps, kNeedO | kNeedDout | kNeedLse, nullptr, nullptr, nullptr, o, dout, lse, nullptr,
                        nullptr, nullptr, B, H, N, d, 1.0f, 0, workspace, workspace_bytes);
   if (st != FA_OK) return st;
@@ -265,7 +280,7 @@ extern "C" int fa_bwd_dkdv(const void* q, const void* k, const void* v, const vo
                            int H, int N, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
   BwdLaunch a;
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   int st = prepare_bwd(a, maps, kNeedQKV | kNeedDout | kNeedDkDv, q, k, v, nullptr, dout, nullptr, nullptr, dk, dv,
                        B, H, N, d, scale, causal, workspace, workspace_bytes);
   if (st != FA_OK) return st;
@@ -275,7 +290,7 @@ extern "C" int fa_bwd_dkdv(const void* q, const void* k, const void* v, const vo
 extern "C" int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, const void* workspace,
                                  size_t workspace_bytes, cudaStream_t stream) {
   BwdLaunch a;
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   int st = prepare_bwd(a, maps, kNeedDq, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr,
                        B, H, N, d, scale, 0, workspace, workspace_bytes);
   if (st != FA_OK) return st;

@@ -118,6 +118,11 @@ struct BwdCfg {
   static constexpr int kStages = 2;                   // Q / dO (+ lse2 / D rows) ring
   static constexpr int kKvStages = (D == 64) ? 2 : 1; // K / V buffers (next unit prefetch)
   static constexpr bool kDqAliasesDp = (D == 128);    // no spare TMEM columns at d = 128
+  // At d = 128 the partial is computed transposed, dQ^T = K^T dS^T (TMEM lanes =
+  // head dimension), so a warp's reductions cover contiguous 128-byte rows of
+  // the accumulator; at d = 64 (M = 64 is not used) it is dQ = dS K, staged in
+  // shared memory and added with a tensor reduce-add.
+  static constexpr bool kDqTransposed = (D == 128);
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
   static constexpr int kThreads = 320;
@@ -132,7 +137,11 @@ struct BwdCfg {
   static constexpr int kOffQ = kOffV + kKvStages * kTileBytes;    // [stages]
   static constexpr int kOffDO = kOffQ + kStages * kTileBytes;     // [stages]
   static constexpr int kOffDS = kOffDO + kStages * kTileBytes;    // 128 x 128 bf16, two swizzle blocks
-  static constexpr int kOffRow = kOffDS + 2 * kSwzBlockBytes;     // [stages][lse2 128 | D 128] fp32
+  // d = 64: two staging buffers of the dQ partial (128 rows x 64 fp32, as two
+  // 128-byte-swizzled 32-column boxes) for the tensor reduce-add.
+  static constexpr int kDqStageBytes = kDqTransposed ? 0 : 2 * kTileRows * D * 4;
+  static constexpr int kOffDQS = kOffDS + 2 * kSwzBlockBytes;
+  static constexpr int kOffRow = kOffDQS + kDqStageBytes;        // [stages][lse2 128 | D 128] fp32
   static constexpr int kRowBytes = 2 * kTileRows * 4;
   static constexpr int kOffBar = kOffRow + kStages * kRowBytes;
   static constexpr int kNumBars = 2 * kKvStages + 3 * kStages + 10;
@@ -164,7 +173,8 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const float* __restrict__ lse2, const float* __restrict__ dsum, float* __restrict__ dq_acc,
+                const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ lse2,
+                const float* __restrict__ dsum, float* __restrict__ dq_acc,
                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int N, int Npad, float c2,
                 float scale, int* status) {
   using C = BwdCfg<D>;
@@ -293,7 +303,7 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T: both K-major over d
       constexpr uint32_t kIdKV = idesc_bf16(128, D, 0, 1);    // dV, dK: B (dO / Q) MN-major
-      constexpr uint32_t kIdQ = idesc_bf16(128, D, 1, 1);     // dQ: A (dS) and B (K) MN-major
+      constexpr uint32_t kIdQ = idesc_bf16(128, C::kDqTransposed ? 128 : D, 1, 1);  // dQ / dQ^T: A, B MN-major
       const uint32_t q_s = smem_addr(sm + C::kOffQ);
       const uint32_t do_s = smem_addr(sm + C::kOffDO);
       const uint32_t ds_s = smem_addr(sm + C::kOffDS);
@@ -374,9 +384,14 @@ __global__ void __launch_bounds__(320, 1)
             mma_ss(tbase + C::kColDK, sdesc(kmajor(ds_s, k), 16, 1024),
                    sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
 #pragma unroll
-          for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ss(tbase + C::kColDQ, sdesc(ds_s + k * 2048, kSwzBlockBytes, 1024),
-                   sdesc(k_s + k * 2048, kSwzBlockBytes, 1024), kIdQ, k > 0);
+          for (int k = 0; k < kTileRows / 16; ++k) {
+            const uint64_t dsd = sdesc(ds_s + k * 2048, kSwzBlockBytes, 1024);  // dS^T, 16 keys
+            const uint64_t kd = sdesc(k_s + k * 2048, kSwzBlockBytes, 1024);    // K, 16 keys
+            if (C::kDqTransposed)
+              mma_ss(tbase + C::kColDQ, kd, dsd, kIdQ, k > 0);  // dQ^T = K^T dS^T
+            else
+              mma_ss(tbase + C::kColDQ, dsd, kd, kIdQ, k > 0);  // dQ = dS K
+          }
           mma_commit(dq_full);
           mma_commit(ds_empty);
           mma_commit(&qdo_empty[st]);
@@ -403,7 +418,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lanes = (uint32_t)quarter * 32;
     const uint32_t t_s = tmem_lane_col(tbase, lanes, C::kColS + 64 * g);
     const uint32_t t_dp = tmem_lane_col(tbase, lanes, C::kColDP + 64 * g);
-    const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + (D / 2) * g);
+    const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + (C::kDqTransposed ? 64 : D / 2) * g);
     const uint32_t t_dv = tmem_lane_col(tbase, lanes, C::kColDV + (D / 2) * g);
     const uint32_t t_dk = tmem_lane_col(tbase, lanes, C::kColDK + (D / 2) * g);
     uint8_t* ds_row = sm + C::kOffDS + g * kSwzBlockBytes + r * 128;
@@ -413,27 +428,53 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     Tracer tr(warp == 0 ? 0 : -1);
 
-    // Read this warpgroup's half of dQ partial of query tile `qt` from TMEM,
-    // release the columns, then add it into the fp32 accumulator.
+    // Read this warpgroup's half of the dQ partial of query tile `qt` from
+    // TMEM, release the columns, then add it into the fp32 accumulator.
     auto drain_dq = [&](int bh, int qt) -> bool {
       tr(40);
       if (!mbar_wait_warp(dq_full, dqcnt & 1, status)) return false;
       ++dqcnt;
       tc_fence_after();
-      uint32_t v[D / 2];
+      if (C::kDqTransposed) {
+        // lane = head-dimension index r, columns = queries 64 g .. 64 g + 63:
+        // one scalar reduction per query, 128 contiguous bytes per warp.
+        uint32_t v[64];
+        tmem_ld32(t_dq, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(t_dq + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        tr(41);
+        const int q0 = qt * kTileRows + 64 * g;
+        float* dst = dq_acc + ((size_t)bh * N + q0) * D + r;
+        const int nvalid = N - q0;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) tmem_ld32(t_dq + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      tr(41);
-      const int q = qt * kTileRows + r;
-      if (q < N) {
-        float* dst = dq_acc + ((size_t)bh * N + q) * D + (D / 2) * g;
+        for (int c = 0; c < 64; ++c)
+          if (c < nvalid) red_add(dst + (size_t)c * D, __uint_as_float(v[c]));
+      } else {
+        // lane = query row r, columns = head dimension [32 g, 32 g + 32): staged
+        // into a swizzled 32-column box, then one tensor reduce-add per
+        // warpgroup (rows past N are clipped by the copy).
+        uint8_t* stage = sm + C::kOffDQS + (dqcnt & 1) * (C::kDqStageBytes / 2) + g * (C::kDqStageBytes / 4);
+        const bool elected = (quarter == 0) && (lane == 0);
+        if (elected) tma_store_wait_read1();  // this buffer's previous reduce has read it
+        named_bar_sync(1 + g, 128);
+        uint32_t v[32];
+        tmem_ld32(t_dq, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        tr(41);
 #pragma unroll
-        for (int m = 0; m < D / 8; ++m)
-          red_add_v4(dst + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
-                     __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
+        for (int m = 0; m < 8; ++m)
+          *reinterpret_cast<uint4*>(stage + r * 128 + ((m ^ swz) * 16)) =
+              make_uint4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1 + g, 128);
+        if (elected) {
+          tma_reduce_add_3d(&tm_dqacc, stage, 32 * g, qt * kTileRows, bh);
+          tma_store_commit();
+        }
       }
       return true;
     };
@@ -564,6 +605,8 @@ __global__ void __launch_bounds__(320, 1)
       if (aborted(abort_flag)) ok = false;
     }
     if (!ok) *abort_flag = 1;
+    // Reductions still in flight must land before the CTA exits.
+    if (!C::kDqTransposed && quarter == 0 && lane == 0) tma_store_wait_all0();
   }
 
   tc_fence_before();
@@ -581,7 +624,8 @@ static cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
   auto kern = fa_bwd_main<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, a.lse2, a.dsum,
+  kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, a.lse2,
+                                                       a.dsum,
                                                        a.dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dk),
                                                        reinterpret_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.Npad,
                                                        a.c2, a.scale, a.status);

@@ -31,6 +31,15 @@
 
 namespace fa {
 
+// Tuning knob: one exp2 pair in kPolyEvery takes the FMA-pipe polynomial
+// instead of MUFU (0 = MUFU only).  Measured on GB300, every fraction tried
+// (1/2, 1/4, 1/8) was slower than MUFU alone: the softmax is bound by issue
+// and latency, not by the MUFU rate, so the default is 0.
+#ifndef FA_FWD_POLY_EVERY
+#define FA_FWD_POLY_EVERY 0
+#endif
+constexpr int kPolyEvery = FA_FWD_POLY_EVERY;
+
 template <int D>
 struct FwdCfg {
   static constexpr int kStages = (D == 128) ? 2 : 4;
@@ -415,7 +424,7 @@ __global__ void __launch_bounds__(320, 1)
             const int c = 32 * h + 2 * i;
             const uint64_t x = f2_fma(f2_pack(s[c], s[c + 1]), c2x2, negm);
             uint64_t p;
-            if (use_poly && (i & 3) == 3) {
+            if (kPolyEvery > 0 && use_poly && (i % kPolyEvery) == kPolyEvery - 1) {
               p = ex2_poly2(x);
             } else {
               float x0, x1;

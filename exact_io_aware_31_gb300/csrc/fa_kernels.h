@@ -25,6 +25,7 @@ struct BwdLaunch {
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_v;
   const CUtensorMap* tm_do;
+  const CUtensorMap* tm_dqacc;  // fp32 [BH, N, d] accumulator, 32-column boxes (d = 64 path)
   const void* o;
   const void* dout;
   const float* lse;
