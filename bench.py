@@ -61,6 +61,21 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, device):
+    """Largest value of ``x`` over all ranks (``x`` itself when not distributed)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Throughput of all ranks together: every rank runs one replica step in ``ms_per_step``."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -207,7 +222,7 @@ def run_ours(args, w):
     build.build()
     fa.load_library()
 
-    q, k, v, do = workloads.workload_inputs(w)
+    q, k, v, do = workloads.workload_inputs(w, rank=rank)  # each rank: its own batch
     B, H, N, d = w.B, w.H, w.N, w.d
     dev = torch.device("cuda", local)
     qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
@@ -294,13 +309,9 @@ def run_ours(args, w):
         kern["fa_bwd_main"] = [e[2].elapsed_time(e[3]) for e in events]
         kern["fa_bwd_dq_conv"] = [e[3].elapsed_time(e[4]) for e in events]
     kern_avg = {k_: sum(v_) / len(v_) for k_, v_ in kern.items()}
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-
+    ms_per_step = max_over_ranks(ms_per_step, dev)
     fwd_f, bwd_f = flops_per_step(w)
-    value = world * (fwd_f + bwd_f) / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, fwd_f + bwd_f, ms_per_step)
 
     # ---- end to end: pinned host buffers in, results out, same C ABI ----
     hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
@@ -336,11 +347,8 @@ def run_ours(args, w):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = whole_job_tflops(world, fwd_f + bwd_f, e2e_ms)
     check(fa.fa_get_device_status(sh), "e2e")
 
     if rank != 0:

@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(320, 1)
           tr(12);
           ok = mbar_wait(&do_full[st], ph, status);
           if (ok && C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
+          tr(18);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -364,10 +365,12 @@ __global__ void __launch_bounds__(320, 1)
           for (int k = 0; k < kTileRows / 16; ++k)
             mma_ts(tbase + C::kColDV, tbase + C::kColS + pt_col(k),
                    sdesc(do_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+          tr(19);
           // S^T(i+1) as early as possible
           if (x + 1 < u.nq) {
             const int st2 = (it + 1) % C::kStages;
             ok = mbar_wait(&q_full[st2], ((it + 1) / C::kStages) & 1, status);
+            tr(20);
             if (!ok) break;
             tc_fence_after();
             issue_st(st2);
@@ -377,6 +380,7 @@ __global__ void __launch_bounds__(320, 1)
           ok = mbar_wait(ds_full, dscnt & 1, status);
           ++dscnt;
           if (ok && !C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
+          tr(16);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -531,7 +535,9 @@ __global__ void __launch_bounds__(320, 1)
         // ---- dQ partial of the previous query tile ----
         if (x > 0 && !(ok = drain_dq(u.bh, i - 1))) break;
         // ---- dS^T = P^T (dP^T - D) -> shared memory (bf16, swizzled) ----
+        tr(42);
         ok = mbar_wait_warp(dp_full, dpcnt & 1, status);
+        tr(43);
         ++dpcnt;
         if (ok) ok = mbar_wait_warp(ds_empty, (dse & 1) ^ 1, status);
         ++dse;

@@ -40,6 +40,13 @@ namespace fa {
 #endif
 constexpr int kPolyEvery = FA_FWD_POLY_EVERY;
 
+#ifdef FA_TEST_HOOKS
+// Test builds only (-DFA_TEST_HOOKS, never the default library): when set,
+// softmax warpgroup 0 withholds its first "P ready" arrival of every unit, so
+// the MMA warp's bounded wait runs out and the failure-detection path runs.
+static __device__ int g_fa_test_withhold_arrival;
+#endif
+
 template <int D>
 struct FwdCfg {
   static constexpr int kStages = (D == 128) ? 2 : 4;
@@ -446,7 +453,12 @@ __global__ void __launch_bounds__(320, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&B.p_full[t]);
+#ifdef FA_TEST_HOOKS
+        const bool withhold = t == 0 && j == 0 && *reinterpret_cast<volatile int*>(&g_fa_test_withhold_arrival) != 0;
+#else
+        constexpr bool withhold = false;
+#endif
+        if (!withhold) mbar_arrive(&B.p_full[t]);
         tr(5);
       }
       if (!ok) break;
@@ -511,6 +523,13 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
 int fwd_units(int BH, int N) { return BH * ((N + 2 * kTileRows - 1) / (2 * kTileRows)); }
 
 }  // namespace fa
+
+#ifdef FA_TEST_HOOKS
+// Test builds only: switch the withheld-arrival hook on (1) or off (0).
+extern "C" int fa_test_withhold_arrival(int on) {
+  return cudaMemcpyToSymbol(fa::g_fa_test_withhold_arrival, &on, sizeof(int)) == cudaSuccess ? 0 : 4;
+}
+#endif
 
 #ifdef FA_TRACE
 // Trace builds only: phase records of this file's kernels.

@@ -98,5 +98,11 @@ def make_inputs(B, H, N, d, seed, stress=None):
     return tuple(t.to(torch.bfloat16) for t in (q, k, v, do))
 
 
-def workload_inputs(w: Workload, stress=None):
-    return make_inputs(w.B, w.H, w.N, w.d, w.seed, stress)
+def replica_seed(w: Workload, rank: int = 0) -> int:
+    """Seed of rank ``rank``'s batch: rank 0 draws the workload's own inputs,
+    every other rank an independent batch of the same shape."""
+    return w.seed + 100003 * rank
+
+
+def workload_inputs(w: Workload, stress=None, rank: int = 0):
+    return make_inputs(w.B, w.H, w.N, w.d, replica_seed(w, rank), stress)
