@@ -26,11 +26,13 @@
 //               dS^T = P^T (dP^T - D) -> shared memory (bf16, 128-byte
 //               swizzled, for dK and dQ); after P of tile i they also read
 //               half of tile i-1's dQ partial from TMEM (thread = query row),
-//               release it and reduce it into the fp32 accumulator; their
-//               half of the dK/dV epilogue
+//               release it and reduce it into the fp32 accumulator (d = 64);
+//               their half of the dK/dV epilogue
 //   warp  8     TMA producer (K/V per unit, double-buffered at d = 64;
 //               Q, dO and their lse2 / D rows per query tile)
 //   warp  9     TMEM owner and MMA issuer
+//   warps 10-13 (d = 128) dQ warpgroup, thread = head-dimension index: reads
+//               each dQ^T partial, releases it, and issues its reductions
 // Tensor memory (512 columns): S^T [0,128) with P^T over [0,32) and
 // [64,96); dP^T [128,256); dV [256,256+d); dK [256+d, 256+2d); the dQ
 // partial in [384,448) at d = 64, and over dP^T at d = 128 (no columns left).
@@ -47,6 +49,14 @@
 #include "sm103_ptx.cuh"
 
 namespace fa {
+
+// Tuning knob: at d = 128, drain the dQ partial with a dedicated warpgroup (1)
+// or from the compute warpgroups (0).  Measured on GB300 the dedicated
+// warpgroup was slower (its 128-register rows cap the whole CTA at 128
+// registers and it still serialises the next dP^T behind its reductions).
+#ifndef FA_BWD_DQ_WARPGROUP
+#define FA_BWD_DQ_WARPGROUP 0
+#endif
 
 // ------------------------------------------------------------ preprocess ----
 // One warp per group of rows: 8 bf16 (16 bytes) per lane.
@@ -125,7 +135,11 @@ struct BwdCfg {
   static constexpr bool kDqTransposed = (D == 128);
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
-  static constexpr int kThreads = 320;
+  // At d = 128 a dedicated dQ warpgroup (warps 10-13) drains the partial and
+  // issues its reductions, so they overlap the compute warpgroups' work; at
+  // d = 64 the compute warpgroups drain it through shared memory.
+  static constexpr bool kDqWarpgroup = kDqTransposed && (FA_BWD_DQ_WARPGROUP != 0);
+  static constexpr int kThreads = kDqWarpgroup ? 448 : 320;
   static constexpr int kTmemCols = 512;
   static constexpr int kColS = 0;     // S^T; P^T of query half g over columns [64 g, 64 g + 32)
   static constexpr int kColDP = 128;  // dP^T
@@ -155,6 +169,16 @@ struct BwdCfg {
 struct BwdUnit {
   int bh, j;      // slice and key tile
   int i0, nq;     // first query tile and number of query tiles
+  int rot;        // the unit visits its query tiles starting at i0 + rot, wrapping
+  // x-th query tile the unit visits.  Without the causal mask every key tile
+  // of a slice visits all query tiles; starting unit j at tile j keeps the
+  // units that run at the same time off the same dQ rows (reductions to one
+  // L2 line serialise).  Under the mask unit j already starts at its own
+  // diagonal tile j.
+  __device__ __forceinline__ int qtile(int x) const {
+    const int k = x + rot;
+    return i0 + (k >= nq ? k - nq : k);
+  }
 };
 
 __device__ __forceinline__ BwdUnit bwd_decode(int pos, int nkt, bool causal) {
@@ -163,6 +187,7 @@ __device__ __forceinline__ BwdUnit bwd_decode(int pos, int nkt, bool causal) {
   u.j = pos - u.bh * nkt;  // ascending j = heaviest first under the causal mask
   u.i0 = causal ? u.j : 0;
   u.nq = nkt - u.i0;
+  u.rot = causal ? 0 : u.j;
   return u;
 }
 
@@ -170,7 +195,7 @@ __device__ __forceinline__ BwdUnit bwd_decode(int pos, int nkt, bool causal) {
 __device__ __forceinline__ uint32_t pt_col(int k) { return (k < 4) ? 8 * k : 64 + 8 * (k - 4); }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ lse2,
@@ -223,7 +248,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(ds_full, 256);
     mbar_init(ds_empty, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 256);
+    mbar_init(dq_empty, C::kDqWarpgroup ? 128 : 256);
     mbar_init(dkdv_full, 1);
     mbar_init(dkdv_empty, 256);
     mbar_init(mma_done, 1);
@@ -268,7 +293,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         ++ucnt;
         for (int x = 0; x < u.nq && ok; ++x, ++it) {
-          const int i = u.i0 + x;
+          const int i = u.qtile(x);
           const int st = it % C::kStages;
           tr(32);
           ok = mbar_wait(&qdo_empty[st], ((it / C::kStages) & 1) ^ 1, status);
@@ -433,7 +458,8 @@ __global__ void __launch_bounds__(320, 1)
     Tracer tr(warp == 0 ? 0 : -1);
 
     // Read this warpgroup's half of the dQ partial of query tile `qt` from
-    // TMEM, release the columns, then add it into the fp32 accumulator.
+    // TMEM, release the columns, then add it into the fp32 accumulator (used
+    // unless the dedicated dQ warpgroup drains it).
     auto drain_dq = [&](int bh, int qt) -> bool {
       tr(40);
       if (!mbar_wait_warp(dq_full, dqcnt & 1, status)) return false;
@@ -491,7 +517,7 @@ __global__ void __launch_bounds__(320, 1)
       const int kr = u.j * kTileRows + r;  // this thread's key
       const bool key_ok = kr < N;
       for (int x = 0; x < u.nq; ++x, ++qit) {
-        const int i = u.i0 + x;
+        const int i = u.qtile(x);
         const int qbase = i * kTileRows + 64 * g;  // first query of this warpgroup's columns
         const bool diag = CAUSAL && (i == u.j);
         // -lse2 / -D of this query tile, staged in shared memory with Q / dO
@@ -533,7 +559,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_arrive(p_full);
         tr(3);
         // ---- dQ partial of the previous query tile ----
-        if (x > 0 && !(ok = drain_dq(u.bh, i - 1))) break;
+        if (!C::kDqWarpgroup && x > 0 && !(ok = drain_dq(u.bh, u.qtile(x - 1)))) break;
         // ---- dS^T = P^T (dP^T - D) -> shared memory (bf16, swizzled) ----
         tr(42);
         ok = mbar_wait_warp(dp_full, dpcnt & 1, status);
@@ -574,7 +600,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (!ok) break;
       // ---- dQ partial of the unit's last query tile ----
-      if (!(ok = drain_dq(u.bh, u.i0 + u.nq - 1))) break;
+      if (!C::kDqWarpgroup && !(ok = drain_dq(u.bh, u.qtile(u.nq - 1)))) break;
       // ---- epilogue: this warpgroup's half of the dV, dK (x scale) columns -> bf16 ----
       tr(6);
       ok = mbar_wait_warp(dkdv_full, ucnt & 1, status);
@@ -613,6 +639,47 @@ __global__ void __launch_bounds__(320, 1)
     if (!ok) *abort_flag = 1;
     // Reductions still in flight must land before the CTA exits.
     if (!C::kDqTransposed && quarter == 0 && lane == 0) tma_store_wait_all0();
+  } else if (C::kDqWarpgroup) {
+    // ------------------------------------------- dQ warpgroup (d = 128) --
+    // Thread = head-dimension index r.  For each query tile it reads the whole
+    // dQ^T row (128 queries) from TMEM, releases the columns at once, then adds
+    // it into the fp32 accumulator: per query, a warp covers 128 contiguous
+    // bytes.  Only this warpgroup waits on the reductions.
+    const int quarter = warp % 4;
+    const int r = quarter * 32 + lane;
+    const uint32_t t_dq = tmem_lane_col(tbase, quarter * 32, C::kColDQ);
+    uint32_t qcnt = 0;
+    bool ok = true;
+    Tracer tr(warp == 12 ? 1 : -1);
+    for (int round = 0; ok; ++round) {
+      if (round * grid >= total_units) break;
+      const int pos = snake_unit(round, blockIdx.x, grid);
+      if (pos >= total_units) continue;
+      const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
+      for (int x = 0; x < u.nq && ok; ++x) {
+        tr(40);
+        ok = mbar_wait_warp(dq_full, qcnt & 1, status);
+        ++qcnt;
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(t_dq + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        tr(41);
+        const int q0 = u.qtile(x) * kTileRows;
+        const int nvalid = N - q0;
+        float* dst = dq_acc + ((size_t)u.bh * N + q0) * D + r;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < nvalid) red_add(dst + (size_t)c * D, __uint_as_float(v[c]));
+        tr(42);
+      }
+      if (aborted(abort_flag)) ok = false;
+    }
+    if (!ok) *abort_flag = 1;
   }
 
   tc_fence_before();

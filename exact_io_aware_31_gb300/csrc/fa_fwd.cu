@@ -302,6 +302,7 @@ __global__ void __launch_bounds__(320, 1)
               if (!ok) break;
               v_ready = true;
             }
+            tr(26 + t);
             tc_fence_after();
             // O_t (+)= P_t V_j : A = P_t from TMEM (8 columns per 16 keys), B = V_j MN-major
             const uint32_t va = v_s + st * C::kTileBytes;
@@ -309,6 +310,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int k = 0; k < kTileRows / 16; ++k)
               mma_ts(tbase + C::kColO + D * t, tbase + C::kColS + 128 * t + k * 8,
                      sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
+            tr(28 + t);
             if (j + 1 < u.nkv(t)) {
               if (!k_next_ready) {
                 ok = mbar_wait(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
@@ -316,6 +318,7 @@ __global__ void __launch_bounds__(320, 1)
                 tc_fence_after();
                 k_next_ready = true;
               }
+              tr(40 + t);
               issue_s(t, st_next);
               if (j + 2 == u.nkv(t)) mma_commit(&B.q_empty[qbuf[t]]);  // last S_t of the unit
             } else {
