@@ -58,6 +58,13 @@ namespace fa {
 #define FA_BWD_DQ_WARPGROUP 0
 #endif
 
+// Tuning knob: in the backward's P^T = 2^(...) one exp2 pair in
+// kBwdPolyEvery takes the FMA-pipe polynomial instead of MUFU (0 = MUFU only).
+#ifndef FA_BWD_POLY_EVERY
+#define FA_BWD_POLY_EVERY 0
+#endif
+constexpr int kBwdPolyEvery = FA_BWD_POLY_EVERY;
+
 // ------------------------------------------------------------ preprocess ----
 // One warp per group of rows: 8 bf16 (16 bytes) per lane.
 template <int D>
@@ -520,6 +527,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int i = u.qtile(x);
         const int qbase = i * kTileRows + 64 * g;  // first query of this warpgroup's columns
         const bool diag = CAUSAL && (i == u.j);
+        const bool full_tile = (i + 1) * kTileRows <= N;  // no padded queries (their P must stay exactly 0)
         // -lse2 / -D of this query tile, staged in shared memory with Q / dO
         const float* rows =
             reinterpret_cast<const float*>(sm + C::kOffRow + (qit % C::kStages) * C::kRowBytes) + 64 * g;
@@ -540,9 +548,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           for (int e = 0; e < 16; ++e) {
             const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(rows + 32 * c + 2 * e);
             const uint64_t xx = f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2x2, nl2);
-            float x0, x1;
-            f2_unpack(xx, x0, x1);
-            float p0 = ex2(x0), p1 = ex2(x1);
+            float p0, p1;
+            if (kBwdPolyEvery > 0 && full_tile && (e % kBwdPolyEvery) == kBwdPolyEvery - 1) {
+              f2_unpack(ex2_poly2(xx), p0, p1);
+            } else {
+              float x0, x1;
+              f2_unpack(xx, x0, x1);
+              p0 = ex2(x0);
+              p1 = ex2(x1);
+            }
             if (diag) {
               const int q = qbase + 32 * c + 2 * e;
               if (q < kr) p0 = 0.f;

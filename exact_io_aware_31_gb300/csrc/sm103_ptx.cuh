@@ -94,21 +94,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
-// Warp-uniform wait: lane 0 waits (bounded), the verdict is broadcast, and the
-// other lanes then observe the already-completed phase themselves (bounded
-// too), so every lane leaves together and with acquire ordering.
+// Warp-uniform wait: every lane tests the barrier itself (acquire) and the warp
+// leaves together once all lanes have seen the phase complete, so the fast
+// path costs one test and one vote.  The time limit is checked by lane 0 and
+// broadcast, so a timeout is also warp-uniform.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status) {
-  const int lane = threadIdx.x & 31;
-  bool ok = true;
-  if (lane == 0) ok = mbar_wait(bar, parity, status);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  if (ok && lane != 0) {
-    const uint32_t a = smem_addr(bar);
-    for (int i = 0; i < (1 << 20) && !mbar_test(a, parity); ++i) {
+  const uint32_t a = smem_addr(bar);
+  bool done = mbar_test(a, parity);
+  if (__all_sync(0xffffffffu, done)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i) {
+      done = done || mbar_test(a, parity);
+      if (__all_sync(0xffffffffu, done)) return true;
+    }
+    const bool expired = __shfl_sync(0xffffffffu, (global_ns() - t0 > kWaitLimitNs) ? 1 : 0, 0) != 0;
+    if (expired) {
+      if ((threadIdx.x & 31) == 0) atomicExch(status, kDevTimeout);
+      return false;
     }
   }
-  __syncwarp();
-  return ok;
 }
 
 // ------------------------------------------------------------------ fences --
