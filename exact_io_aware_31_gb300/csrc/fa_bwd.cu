@@ -279,27 +279,50 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
       tma_prefetch_map(&tm_do);
-      uint32_t ucnt = 0, it = 0;
+      uint32_t ucnt = 0, it = 0;  // K/V copies issued (one per unit, in unit order); Q/dO tiles issued
       bool ok = true;
+      // K/V of the unit at `p` into buffer ucnt % kKvStages (waits for the buffer).
+      auto issue_kv = [&](int p) -> bool {
+        const BwdUnit v = bwd_decode(p, nkt, CAUSAL);
+        const int kb = ucnt % C::kKvStages;
+        tr(30);
+        if (!mbar_wait(&kv_empty[kb], ((ucnt / C::kKvStages) & 1) ^ 1, status)) return false;
+        tr(31);
+        mbar_expect_tx(&kv_full[kb], 2 * C::kTileBytes);
+        for (int b = 0; b < C::kBlocks; ++b) {
+          tma_load_3d(sm + C::kOffK + kb * C::kTileBytes + b * kSwzBlockBytes, &tm_k, &kv_full[kb], b * 64,
+                      v.j * kTileRows, v.bh);
+          tma_load_3d(sm + C::kOffV + kb * C::kTileBytes + b * kSwzBlockBytes, &tm_v, &kv_full[kb], b * 64,
+                      v.j * kTileRows, v.bh);
+        }
+        ++ucnt;
+        return true;
+      };
+      // Next unit this CTA will process after round r, or -1.
+      auto next_pos = [&](int r) -> int {
+        for (int rr = r + 1; rr * grid < total_units; ++rr) {
+          const int p = snake_unit(rr, blockIdx.x, grid);
+          if (p < total_units) return p;
+        }
+        return -1;
+      };
+      int prefetched = -1;  // unit whose K/V copy was issued ahead of its turn
       for (int round = 0; ok; ++round) {
         if (round * grid >= total_units) break;
         const int pos = snake_unit(round, blockIdx.x, grid);
         if (pos >= total_units) continue;
         const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
-        const int kb = ucnt % C::kKvStages;
-        tr(30);
-        ok = mbar_wait(&kv_empty[kb], ((ucnt / C::kKvStages) & 1) ^ 1, status);
-        tr(31);
-        if (!ok) break;
-        mbar_expect_tx(&kv_full[kb], 2 * C::kTileBytes);
-        for (int b = 0; b < C::kBlocks; ++b) {
-          tma_load_3d(sm + C::kOffK + kb * C::kTileBytes + b * kSwzBlockBytes, &tm_k, &kv_full[kb], b * 64,
-                      u.j * kTileRows, u.bh);
-          tma_load_3d(sm + C::kOffV + kb * C::kTileBytes + b * kSwzBlockBytes, &tm_v, &kv_full[kb], b * 64,
-                      u.j * kTileRows, u.bh);
-        }
-        ++ucnt;
+        if (prefetched != pos && !(ok = issue_kv(pos))) break;
+        prefetched = -1;
+        // With two K/V buffers the next unit's copy goes out as soon as its
+        // buffer is released, between this unit's Q / dO copies.
+        const int npos = (C::kKvStages > 1) ? next_pos(round) : -1;
         for (int x = 0; x < u.nq && ok; ++x, ++it) {
+          if (npos >= 0 && prefetched < 0 &&
+              mbar_probe(smem_addr(&kv_empty[ucnt % C::kKvStages]), ((ucnt / C::kKvStages) & 1) ^ 1)) {
+            if (!(ok = issue_kv(npos))) break;
+            prefetched = npos;
+          }
           const int i = u.qtile(x);
           const int st = it % C::kStages;
           tr(32);
@@ -461,6 +484,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int swz = r & 7;
     const uint64_t c2x2 = f2_pack(c2, c2);
     uint32_t scnt = 0, dpcnt = 0, dse = 0, ucnt = 0, qit = 0, dqcnt = 0;
+    int pend_bh = 0, pend_qt = -1;  // dQ partial still to drain from the previous unit
     bool ok = true;
     Tracer tr(warp == 0 ? 0 : -1);
 
@@ -573,7 +597,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_arrive(p_full);
         tr(3);
         // ---- dQ partial of the previous query tile ----
-        if (!C::kDqWarpgroup && x > 0 && !(ok = drain_dq(u.bh, u.qtile(x - 1)))) break;
+        if (!C::kDqWarpgroup) {
+          // dQ of the previous query tile: this unit's, or the last one of
+          // the previous unit (deferred so the unit boundary does not wait).
+          if (x > 0) {
+            if (!(ok = drain_dq(u.bh, u.qtile(x - 1)))) break;
+          } else if (pend_qt >= 0) {
+            if (!(ok = drain_dq(pend_bh, pend_qt))) break;
+            pend_qt = -1;
+          }
+        }
         // ---- dS^T = P^T (dP^T - D) -> shared memory (bf16, swizzled) ----
         tr(42);
         ok = mbar_wait_warp(dp_full, dpcnt & 1, status);
@@ -614,7 +647,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
       if (!ok) break;
       // ---- dQ partial of the unit's last query tile ----
-      if (!C::kDqWarpgroup && !(ok = drain_dq(u.bh, u.qtile(u.nq - 1)))) break;
+      if (!C::kDqWarpgroup) {  // the unit's last dQ partial drains after P(0) of the next unit
+        pend_bh = u.bh;
+        pend_qt = u.qtile(u.nq - 1);
+      }
       // ---- epilogue: this warpgroup's half of the dV, dK (x scale) columns -> bf16 ----
       tr(6);
       ok = mbar_wait_warp(dkdv_full, ucnt & 1, status);
@@ -628,6 +664,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tmem_ld32(t_dv + 32 * c, a);
         tmem_ld32(t_dk + 32 * c, b);
         tmem_wait_ld();
+        if (c == D / 64 - 1) {  // dK / dV columns read: the next unit may overwrite them
+          tc_fence_before();
+          mbar_arrive(dkdv_empty);
+        }
         if (key_ok) {
           uint4* dvp = reinterpret_cast<uint4*>(dv + rowoff + 32 * c);
           uint4* dkp = reinterpret_cast<uint4*>(dk + rowoff + 32 * c);
@@ -645,11 +685,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(dkdv_empty);
       tr(7);
       if (aborted(abort_flag)) ok = false;
     }
+    if (ok && pend_qt >= 0) ok = drain_dq(pend_bh, pend_qt);
     if (!ok) *abort_flag = 1;
     // Reductions still in flight must land before the CTA exits.
     if (!C::kDqTransposed && quarter == 0 && lane == 0) tma_store_wait_all0();
