@@ -216,7 +216,11 @@ int prepare_bwd(BwdLaunch& a, CUtensorMap* maps, unsigned need, const void* q, c
   }
   uint8_t* ws = static_cast<uint8_t*>(const_cast<void*>(workspace));
   if ((need & kNeedQKV) && make_map_f32(&maps[4], ws + w.dq_acc, BH, N, d)) return FA_ERR_CUDA;
+  if ((need & kNeedDkDv) && (make_map(&maps[5], dk, BH, N, d) || make_map(&maps[6], dv, BH, N, d)))
+    return FA_ERR_CUDA;
   a.tm_dqacc = &maps[4];
+  a.tm_dk = &maps[5];
+  a.tm_dv = &maps[6];
   a.tm_q = &maps[0];
   a.tm_k = &maps[1];
   a.tm_v = &maps[2];
@@ -257,7 +261,7 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
                       void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   BwdLaunch a;
-  CUtensorMap maps[5];
+  CUtensorMap maps[7];
   int st = prepare_bwd(a, maps, kNeedQKV | kNeedO | kNeedDout | kNeedLse | kNeedDq | kNeedDkDv, q, k, v, o, dout,
                        lse, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes);
   if (st != FA_OK) return st;
@@ -269,7 +273,7 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
 extern "C" int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   BwdLaunch a;
-  CUtensorMap maps[5];
+  CUtensorMap maps[7];
   int st = prepare_bwd(a, maps, kNeedO | kNeedDout | kNeedLse, nullptr, nullptr, nullptr, o, dout, lse, nullptr,
                        nullptr, nullptr, B, H, N, d, 1.0f, 0, workspace, workspace_bytes);
   if (st != FA_OK) return st;
@@ -280,7 +284,7 @@ extern "C" int fa_bwd_dkdv(const void* q, const void* k, const void* v, const vo
                            int H, int N, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
   BwdLaunch a;
-  CUtensorMap maps[5];
+  CUtensorMap maps[7];
   int st = prepare_bwd(a, maps, kNeedQKV | kNeedDout | kNeedDkDv, q, k, v, nullptr, dout, nullptr, nullptr, dk, dv,
                        B, H, N, d, scale, causal, workspace, workspace_bytes);
   if (st != FA_OK) return st;
@@ -290,7 +294,7 @@ extern "C" int fa_bwd_dkdv(const void* q, const void* k, const void* v, const vo
 extern "C" int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, const void* workspace,
                                  size_t workspace_bytes, cudaStream_t stream) {
   BwdLaunch a;
-  CUtensorMap maps[5];
+  CUtensorMap maps[7];
   int st = prepare_bwd(a, maps, kNeedDq, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr,
                        B, H, N, d, scale, 0, workspace, workspace_bytes);
   if (st != FA_OK) return st;

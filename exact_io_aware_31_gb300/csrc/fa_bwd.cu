@@ -64,6 +64,7 @@ namespace fa {
 #define FA_BWD_POLY_EVERY 0
 #endif
 constexpr int kBwdPolyEvery = FA_BWD_POLY_EVERY;
+constexpr int kBwdPolyMod = kBwdPolyEvery > 0 ? kBwdPolyEvery : 1;  // divisor that is never zero
 
 // ------------------------------------------------------------ preprocess ----
 // One warp per group of rows: 8 bf16 (16 bytes) per lane.
@@ -142,10 +143,16 @@ struct BwdCfg {
   static constexpr bool kDqTransposed = (D == 128);
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
-  // At d = 128 a dedicated dQ warpgroup (warps 10-13) drains the partial and
-  // issues its reductions, so they overlap the compute warpgroups' work; at
-  // d = 64 the compute warpgroups drain it through shared memory.
-  static constexpr bool kDqWarpgroup = kDqTransposed && (FA_BWD_DQ_WARPGROUP != 0);
+  // d = 64: a dedicated dQ warpgroup (warps 10-13) drains each partial
+  // through the staging buffers with tensor reduce-adds (asynchronous, so it
+  // never waits on them); d = 128: the compute warpgroups drain it with
+  // coalesced reductions (FA_BWD_DQ_WARPGROUP selects the dedicated
+  // warpgroup there too; it measured slower).
+  static constexpr bool kDqWarpgroup = !kDqTransposed || (FA_BWD_DQ_WARPGROUP != 0);
+  // d = 64: dK / dV leave through the dS buffer (free once the unit's last
+  // MMAs are done) as two 64-column boxes with TMA stores; at d = 128 they
+  // do not fit there and each thread stores its own row.
+  static constexpr bool kEpiTma = (D == 64);
   static constexpr int kThreads = kDqWarpgroup ? 448 : 320;
   static constexpr int kTmemCols = 512;
   static constexpr int kColS = 0;     // S^T; P^T of query half g over columns [64 g, 64 g + 32)
@@ -157,15 +164,22 @@ struct BwdCfg {
   static constexpr int kOffV = kOffK + kKvStages * kTileBytes;
   static constexpr int kOffQ = kOffV + kKvStages * kTileBytes;    // [stages]
   static constexpr int kOffDO = kOffQ + kStages * kTileBytes;     // [stages]
-  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;    // 128 x 128 bf16, two swizzle blocks
-  // d = 64: two staging buffers of the dQ partial (128 rows x 64 fp32, as two
+  // d = 64: dP^T(i+1) is issued as soon as dS(i) is in shared memory (ahead
+  // of dK(i), dQ(i)), and dS is double-buffered so dS(i+1) need not wait for
+  // those two to finish reading dS(i).  At d = 128 the dQ^T partial occupies
+  // the dP^T columns, so dP^T(i+1) waits until dQ^T(i) has been drained.
+  static constexpr bool kEarlyDp = !kDqAliasesDp;
+  static constexpr int kDsBufs = kEarlyDp ? 2 : 1;
+  static constexpr int kDsBytes = 2 * kSwzBlockBytes;              // 128 x 128 bf16 dS^T, two swizzle blocks
+  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;    // [kDsBufs]
+  // d = 64: staging buffer of the dQ partial (128 rows x 64 fp32, as two
   // 128-byte-swizzled 32-column boxes) for the tensor reduce-add.
-  static constexpr int kDqStageBytes = kDqTransposed ? 0 : 2 * kTileRows * D * 4;
-  static constexpr int kOffDQS = kOffDS + 2 * kSwzBlockBytes;
+  static constexpr int kDqStageBytes = kDqTransposed ? 0 : kTileRows * D * 4;
+  static constexpr int kOffDQS = kOffDS + kDsBufs * kDsBytes;
   static constexpr int kOffRow = kOffDQS + kDqStageBytes;        // [stages][lse2 128 | D 128] fp32
   static constexpr int kRowBytes = 2 * kTileRows * 4;
   static constexpr int kOffBar = kOffRow + kStages * kRowBytes;
-  static constexpr int kNumBars = 2 * kKvStages + 3 * kStages + 10;
+  static constexpr int kNumBars = 2 * kKvStages + 3 * kStages + 15;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;
@@ -205,7 +219,8 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ lse2,
+                const __grid_constant__ CUtensorMap tm_dqacc, const __grid_constant__ CUtensorMap tm_dk,
+                const __grid_constant__ CUtensorMap tm_dv, const float* __restrict__ lse2,
                 const float* __restrict__ dsum, float* __restrict__ dq_acc,
                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int N, int Npad, float c2,
                 float scale, int* status) {
@@ -230,6 +245,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   uint64_t* dkdv_full = s_full + 7;
   uint64_t* dkdv_empty = s_full + 8;
   uint64_t* mma_done = s_full + 9;
+  uint64_t* epi_full = s_full + 10;  // d = 64: dK / dV staged in the dS buffer (256 arrivals)
+  uint64_t* epi_free = s_full + 11;  // d = 64: their stores have read the dS buffer
+  uint64_t* dqs_full = s_full + 12;  // d = 64: a dQ partial staged (128 arrivals)
+  uint64_t* dqs_free = s_full + 13;  // d = 64: the staging buffer is free
+  uint64_t* ds_empty2 = s_full + 14;  // second dS buffer (d = 64)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
 
@@ -254,11 +274,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(ds_full, 256);
     mbar_init(ds_empty, 1);
+    mbar_init(ds_empty2, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, C::kDqWarpgroup ? 128 : 256);
     mbar_init(dkdv_full, 1);
     mbar_init(dkdv_empty, 256);
     mbar_init(mma_done, 1);
+    mbar_init(epi_full, 256);
+    mbar_init(epi_free, 1);
+    mbar_init(dqs_full, 128);
+    mbar_init(dqs_free, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -315,18 +340,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (prefetched != pos && !(ok = issue_kv(pos))) break;
         prefetched = -1;
         // With two K/V buffers the next unit's copy goes out as soon as its
-        // buffer is released, between this unit's Q / dO copies.
+        // buffer is released: the wait for a Q / dO slot polls that buffer too.
         const int npos = (C::kKvStages > 1) ? next_pos(round) : -1;
         for (int x = 0; x < u.nq && ok; ++x, ++it) {
-          if (npos >= 0 && prefetched < 0 &&
-              mbar_probe(smem_addr(&kv_empty[ucnt % C::kKvStages]), ((ucnt / C::kKvStages) & 1) ^ 1)) {
-            if (!(ok = issue_kv(npos))) break;
-            prefetched = npos;
-          }
           const int i = u.qtile(x);
           const int st = it % C::kStages;
           tr(32);
-          ok = mbar_wait(&qdo_empty[st], ((it / C::kStages) & 1) ^ 1, status);
+          {
+            const uint32_t qa = smem_addr(&qdo_empty[st]);
+            const uint32_t qp = ((it / C::kStages) & 1) ^ 1;
+            const uint64_t t0 = global_ns();
+            while (true) {
+              if (npos >= 0 && prefetched < 0 &&
+                  mbar_probe(smem_addr(&kv_empty[ucnt % C::kKvStages]), ((ucnt / C::kKvStages) & 1) ^ 1)) {
+                if (!(ok = issue_kv(npos))) break;
+                prefetched = npos;
+              }
+              if (mbar_probe(qa, qp)) break;
+              if (global_ns() - t0 > kWaitLimitNs) {
+                atomicExch(status, kDevTimeout);
+                ok = false;
+                break;
+              }
+            }
+          }
           tr(33);
           if (!ok) break;
           float* rows = reinterpret_cast<float*>(sm + C::kOffRow + st * C::kRowBytes);
@@ -381,33 +418,47 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                    sdesc(kmajor(q_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
           mma_commit(s_full);
         };
+        auto issue_dp = [&](int st) {  // dP^T = V dO^T
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(tbase + C::kColDP, sdesc(kmajor(v_s, k), 16, 1024),
+                   sdesc(kmajor(do_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
+          mma_commit(dp_full);
+        };
         tr(10);
         ok = mbar_wait(&kv_full[kb], (ucnt / C::kKvStages) & 1, status);
         tr(11);
         if (!ok) break;
         {
           const int st = it % C::kStages;
-          ok = mbar_wait(&q_full[st], (it / C::kStages) & 1, status);
+          const uint32_t ph = (it / C::kStages) & 1;
+          ok = mbar_wait(&q_full[st], ph, status);
           if (!ok) break;
           tc_fence_after();
           issue_st(st);
+          if (C::kEarlyDp) {
+            ok = mbar_wait(&do_full[st], ph, status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(st);
+          }
         }
         for (int x = 0; x < u.nq && ok; ++x, ++it) {
           const int st = it % C::kStages;
+          const int st2 = (it + 1) % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
-          // dP^T(i) = V dO^T
-          tr(12);
-          ok = mbar_wait(&do_full[st], ph, status);
-          if (ok && C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
-          tr(18);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss(tbase + C::kColDP, sdesc(kmajor(v_s, k), 16, 1024),
-                   sdesc(kmajor(do_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
-          mma_commit(dp_full);
-          tr(13);
+          const uint32_t ph2 = ((it + 1) / C::kStages) & 1;
+          if (!C::kEarlyDp) {
+            // dP^T(i) once dO(i) is in and the dQ^T partial sharing its columns is drained
+            tr(12);
+            ok = mbar_wait(&do_full[st], ph, status);
+            if (ok) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
+            tr(18);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(st);
+            tr(13);
+          }
           // dV += P^T dO  (A = P^T from TMEM, B = dO MN-major); the first of a unit
           // also waits until the previous unit's dK/dV have been read out.
           ok = mbar_wait(p_full, pcnt & 1, status);
@@ -423,36 +474,47 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           tr(19);
           // S^T(i+1) as early as possible
           if (x + 1 < u.nq) {
-            const int st2 = (it + 1) % C::kStages;
-            ok = mbar_wait(&q_full[st2], ((it + 1) / C::kStages) & 1, status);
+            ok = mbar_wait(&q_full[st2], ph2, status);
             tr(20);
             if (!ok) break;
             tc_fence_after();
             issue_st(st2);
           }
-          // dK += dS^T Q ; dQ_part = dS K
+          // dS(i) in shared memory: [dP^T(i+1)], dK += dS^T Q, dQ_part = dS K
           tr(15);
           ok = mbar_wait(ds_full, dscnt & 1, status);
+          const int db = dscnt % C::kDsBufs;
           ++dscnt;
-          if (ok && !C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
+          if (!ok) break;
+          if (C::kEarlyDp && x + 1 < u.nq) {
+            tr(12);
+            ok = mbar_wait(&do_full[st2], ph2, status);
+            tr(18);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(st2);
+            tr(13);
+          }
+          if (!C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
           tr(16);
           if (!ok) break;
           tc_fence_after();
+          const uint32_t dsb = ds_s + db * C::kDsBytes;
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ss(tbase + C::kColDK, sdesc(kmajor(ds_s, k), 16, 1024),
+            mma_ss(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
                    sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k) {
-            const uint64_t dsd = sdesc(ds_s + k * 2048, kSwzBlockBytes, 1024);  // dS^T, 16 keys
-            const uint64_t kd = sdesc(k_s + k * 2048, kSwzBlockBytes, 1024);    // K, 16 keys
+            const uint64_t dsd = sdesc(dsb + k * 2048, kSwzBlockBytes, 1024);  // dS^T, 16 keys
+            const uint64_t kd = sdesc(k_s + k * 2048, kSwzBlockBytes, 1024);   // K, 16 keys
             if (C::kDqTransposed)
               mma_ss(tbase + C::kColDQ, kd, dsd, kIdQ, k > 0);  // dQ^T = K^T dS^T
             else
               mma_ss(tbase + C::kColDQ, dsd, kd, kIdQ, k > 0);  // dQ = dS K
           }
           mma_commit(dq_full);
-          mma_commit(ds_empty);
+          mma_commit(db ? ds_empty2 : ds_empty);
           mma_commit(&qdo_empty[st]);
           ++dqcnt;
           tr(17);
@@ -480,16 +542,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + (C::kDqTransposed ? 64 : D / 2) * g);
     const uint32_t t_dv = tmem_lane_col(tbase, lanes, C::kColDV + (D / 2) * g);
     const uint32_t t_dk = tmem_lane_col(tbase, lanes, C::kColDK + (D / 2) * g);
-    uint8_t* ds_row = sm + C::kOffDS + g * kSwzBlockBytes + r * 128;
+    uint8_t* ds_row0 = sm + C::kOffDS + g * kSwzBlockBytes + r * 128;  // + buffer * kDsBytes
     const int swz = r & 7;
     const uint64_t c2x2 = f2_pack(c2, c2);
     uint32_t scnt = 0, dpcnt = 0, dse = 0, ucnt = 0, qit = 0, dqcnt = 0;
+    uint32_t ecnt = 0;        // d = 64: units whose dK / dV went out through the dS buffer
+    bool epi_pending = false;  // ... the last of which may still be reading it
     int pend_bh = 0, pend_qt = -1;  // dQ partial still to drain from the previous unit
     bool ok = true;
     Tracer tr(warp == 0 ? 0 : -1);
 
-    // Read this warpgroup's half of the dQ partial of query tile `qt` from
-    // TMEM, release the columns, then add it into the fp32 accumulator (used
+    // Read this warpgroup's half of the dQ^T partial of query tile `qt` from
+    // TMEM, release the columns, then add it into the fp32 accumulator (d = 128
     // unless the dedicated dQ warpgroup drains it).
     auto drain_dq = [&](int bh, int qt) -> bool {
       tr(40);
@@ -512,30 +576,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (c < nvalid) red_add(dst + (size_t)c * D, __uint_as_float(v[c]));
-      } else {
-        // lane = query row r, columns = head dimension [32 g, 32 g + 32): staged
-        // into a swizzled 32-column box, then one tensor reduce-add per
-        // warpgroup (rows past N are clipped by the copy).
-        uint8_t* stage = sm + C::kOffDQS + (dqcnt & 1) * (C::kDqStageBytes / 2) + g * (C::kDqStageBytes / 4);
-        const bool elected = (quarter == 0) && (lane == 0);
-        if (elected) tma_store_wait_read1();  // this buffer's previous reduce has read it
-        named_bar_sync(1 + g, 128);
-        uint32_t v[32];
-        tmem_ld32(t_dq, v);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(dq_empty);
-        tr(41);
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-          *reinterpret_cast<uint4*>(stage + r * 128 + ((m ^ swz) * 16)) =
-              make_uint4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
-        fence_proxy_async_smem();
-        named_bar_sync(1 + g, 128);
-        if (elected) {
-          tma_reduce_add_3d(&tm_dqacc, stage, 32 * g, qt * kTileRows, bh);
-          tma_store_commit();
-        }
       }
       return true;
     };
@@ -573,7 +613,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(rows + 32 * c + 2 * e);
             const uint64_t xx = f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2x2, nl2);
             float p0, p1;
-            if (kBwdPolyEvery > 0 && full_tile && (e % kBwdPolyEvery) == kBwdPolyEvery - 1) {
+            if (kBwdPolyEvery > 0 && full_tile && (e % kBwdPolyMod) == kBwdPolyMod - 1) {
               f2_unpack(ex2_poly2(xx), p0, p1);
             } else {
               float x0, x1;
@@ -612,8 +652,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         ok = mbar_wait_warp(dp_full, dpcnt & 1, status);
         tr(43);
         ++dpcnt;
-        if (ok) ok = mbar_wait_warp(ds_empty, (dse & 1) ^ 1, status);
+        const int db = dse % C::kDsBufs;
+        if (ok) ok = mbar_wait_warp(db ? ds_empty2 : ds_empty, ((dse / C::kDsBufs) & 1) ^ 1, status);
         ++dse;
+        uint8_t* ds_row = ds_row0 + db * C::kDsBytes;
+        if (ok && C::kEpiTma && epi_pending) {  // the previous unit's dK / dV stores read the buffer
+          if (warp == 0 && lane == 0) {
+            tma_store_wait_read0();
+            mbar_arrive(epi_free);
+          }
+          ok = mbar_wait_warp(epi_free, (ecnt - 1) & 1, status);
+          epi_pending = false;
+        }
         tr(4);
         if (!ok) break;
         tc_fence_after();
@@ -657,31 +707,73 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ++ucnt;
       if (!ok) break;
       tc_fence_after();
-      const size_t rowoff = ((size_t)u.bh * N + kr) * D + (D / 2) * g;
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
+      if (C::kEpiTma) {
+        // dV, dK (x scale) -> bf16 in the dS buffer as 128-byte-swizzled
+        // 64-column boxes (block 0 dV, block 1 dK; this warpgroup writes
+        // columns [32 g, 32 g + 32) of its key row), then one thread stores
+        // both boxes.  Rows past N are clipped by the copy.
         uint32_t a[32], b[32];
-        tmem_ld32(t_dv + 32 * c, a);
-        tmem_ld32(t_dk + 32 * c, b);
+        tmem_ld32(t_dv, a);
+        tmem_ld32(t_dk, b);
         tmem_wait_ld();
-        if (c == D / 64 - 1) {  // dK / dV columns read: the next unit may overwrite them
-          tc_fence_before();
-          mbar_arrive(dkdv_empty);
-        }
-        if (key_ok) {
-          uint4* dvp = reinterpret_cast<uint4*>(dv + rowoff + 32 * c);
-          uint4* dkp = reinterpret_cast<uint4*>(dk + rowoff + 32 * c);
+        tc_fence_before();
+        mbar_arrive(dkdv_empty);  // the next unit may overwrite the columns
+        uint8_t* rv = sm + C::kOffDS + r * 128;
+        uint8_t* rk = rv + kSwzBlockBytes;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            dvp[m] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * m]), __uint_as_float(a[8 * m + 1])),
-                                pack_bf16x2(__uint_as_float(a[8 * m + 2]), __uint_as_float(a[8 * m + 3])),
-                                pack_bf16x2(__uint_as_float(a[8 * m + 4]), __uint_as_float(a[8 * m + 5])),
-                                pack_bf16x2(__uint_as_float(a[8 * m + 6]), __uint_as_float(a[8 * m + 7])));
-            dkp[m] = make_uint4(
-                pack_bf16x2(__uint_as_float(b[8 * m]) * scale, __uint_as_float(b[8 * m + 1]) * scale),
-                pack_bf16x2(__uint_as_float(b[8 * m + 2]) * scale, __uint_as_float(b[8 * m + 3]) * scale),
-                pack_bf16x2(__uint_as_float(b[8 * m + 4]) * scale, __uint_as_float(b[8 * m + 5]) * scale),
-                pack_bf16x2(__uint_as_float(b[8 * m + 6]) * scale, __uint_as_float(b[8 * m + 7]) * scale));
+        for (int m = 0; m < 4; ++m) {
+          const int ch = ((4 * g + m) ^ swz) * 16;
+          *reinterpret_cast<uint4*>(rv + ch) =
+              make_uint4(pack_bf16x2(__uint_as_float(a[8 * m]), __uint_as_float(a[8 * m + 1])),
+                         pack_bf16x2(__uint_as_float(a[8 * m + 2]), __uint_as_float(a[8 * m + 3])),
+                         pack_bf16x2(__uint_as_float(a[8 * m + 4]), __uint_as_float(a[8 * m + 5])),
+                         pack_bf16x2(__uint_as_float(a[8 * m + 6]), __uint_as_float(a[8 * m + 7])));
+          *reinterpret_cast<uint4*>(rk + ch) =
+              make_uint4(pack_bf16x2(__uint_as_float(b[8 * m]) * scale, __uint_as_float(b[8 * m + 1]) * scale),
+                         pack_bf16x2(__uint_as_float(b[8 * m + 2]) * scale, __uint_as_float(b[8 * m + 3]) * scale),
+                         pack_bf16x2(__uint_as_float(b[8 * m + 4]) * scale, __uint_as_float(b[8 * m + 5]) * scale),
+                         pack_bf16x2(__uint_as_float(b[8 * m + 6]) * scale, __uint_as_float(b[8 * m + 7]) * scale));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(epi_full);
+        if (warp == 0) {
+          ok = mbar_wait_warp(epi_full, ecnt & 1, status);
+          if (ok && lane == 0) {
+            tma_store_3d(&tm_dv, sm + C::kOffDS, 0, u.j * kTileRows, u.bh);
+            tma_store_3d(&tm_dk, sm + C::kOffDS + kSwzBlockBytes, 0, u.j * kTileRows, u.bh);
+            tma_store_commit();
+          }
+        }
+        ++ecnt;
+        epi_pending = true;
+        if (!ok) break;
+      } else {
+        const size_t rowoff = ((size_t)u.bh * N + kr) * D + (D / 2) * g;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t a[32], b[32];
+          tmem_ld32(t_dv + 32 * c, a);
+          tmem_ld32(t_dk + 32 * c, b);
+          tmem_wait_ld();
+          if (c == D / 64 - 1) {  // dK / dV columns read: the next unit may overwrite them
+            tc_fence_before();
+            mbar_arrive(dkdv_empty);
+          }
+          if (key_ok) {
+            uint4* dvp = reinterpret_cast<uint4*>(dv + rowoff + 32 * c);
+            uint4* dkp = reinterpret_cast<uint4*>(dk + rowoff + 32 * c);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              dvp[m] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * m]), __uint_as_float(a[8 * m + 1])),
+                                  pack_bf16x2(__uint_as_float(a[8 * m + 2]), __uint_as_float(a[8 * m + 3])),
+                                  pack_bf16x2(__uint_as_float(a[8 * m + 4]), __uint_as_float(a[8 * m + 5])),
+                                  pack_bf16x2(__uint_as_float(a[8 * m + 6]), __uint_as_float(a[8 * m + 7])));
+              dkp[m] = make_uint4(
+                  pack_bf16x2(__uint_as_float(b[8 * m]) * scale, __uint_as_float(b[8 * m + 1]) * scale),
+                  pack_bf16x2(__uint_as_float(b[8 * m + 2]) * scale, __uint_as_float(b[8 * m + 3]) * scale),
+                  pack_bf16x2(__uint_as_float(b[8 * m + 4]) * scale, __uint_as_float(b[8 * m + 5]) * scale),
+                  pack_bf16x2(__uint_as_float(b[8 * m + 6]) * scale, __uint_as_float(b[8 * m + 7]) * scale));
+            }
           }
         }
       }
@@ -690,17 +782,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     if (ok && pend_qt >= 0) ok = drain_dq(pend_bh, pend_qt);
     if (!ok) *abort_flag = 1;
-    // Reductions still in flight must land before the CTA exits.
-    if (!C::kDqTransposed && quarter == 0 && lane == 0) tma_store_wait_all0();
+    // dK / dV stores still in flight must finish before the CTA exits.
+    if (C::kEpiTma && warp == 0 && lane == 0) tma_store_wait_all0();
   } else if (C::kDqWarpgroup) {
-    // ------------------------------------------- dQ warpgroup (d = 128) --
-    // Thread = head-dimension index r.  For each query tile it reads the whole
-    // dQ^T row (128 queries) from TMEM, releases the columns at once, then adds
-    // it into the fp32 accumulator: per query, a warp covers 128 contiguous
-    // bytes.  Only this warpgroup waits on the reductions.
+    // ----------------------------------------------------- dQ warpgroup --
+    // d = 128 (transposed partial): thread = head-dimension index r; it reads
+    // the whole dQ^T row (128 queries), releases the columns, then reduces it
+    // into the accumulator (per query a warp covers 128 contiguous bytes).
+    // d = 64: thread = query row r; it reads its 64-column dQ row, releases
+    // the columns, writes the row into a pair of 128-byte-swizzled 32-column
+    // boxes, and one thread issues the tensor reduce-adds.
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;
     const uint32_t t_dq = tmem_lane_col(tbase, quarter * 32, C::kColDQ);
+    const bool elected = (warp == 10) && (lane == 0);
     uint32_t qcnt = 0;
     bool ok = true;
     Tracer tr(warp == 12 ? 1 : -1);
@@ -715,24 +810,59 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         ++qcnt;
         if (!ok) break;
         tc_fence_after();
-        uint32_t v[128];
+        if (C::kDqTransposed) {
+          uint32_t v[128];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_dq + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(dq_empty);
-        tr(41);
-        const int q0 = u.qtile(x) * kTileRows;
-        const int nvalid = N - q0;
-        float* dst = dq_acc + ((size_t)u.bh * N + q0) * D + r;
+          for (int c = 0; c < 4; ++c) tmem_ld32(t_dq + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(dq_empty);
+          tr(41);
+          const int q0 = u.qtile(x) * kTileRows;
+          const int nvalid = N - q0;
+          float* dst = dq_acc + ((size_t)u.bh * N + q0) * D + r;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c < nvalid) red_add(dst + (size_t)c * D, __uint_as_float(v[c]));
+          for (int c = 0; c < 128; ++c)
+            if (c < nvalid) red_add(dst + (size_t)c * D, __uint_as_float(v[c]));
+        } else {
+          uint8_t* stage = sm + C::kOffDQS;
+          if (elected) {
+            tma_store_wait_read0();  // the previous reduce-adds have read the buffer
+            mbar_arrive(dqs_free);
+          }
+          if (!(ok = mbar_wait_warp(dqs_free, (qcnt - 1) & 1, status))) break;
+          uint32_t v[64];
+          tmem_ld32(t_dq, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(t_dq + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(dq_empty);
+          tr(41);
+          const int swz = r & 7;
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+              *reinterpret_cast<uint4*>(stage + b * (C::kDqStageBytes / 2) + r * 128 + ((m ^ swz) * 16)) =
+                  make_uint4(v[32 * b + 4 * m], v[32 * b + 4 * m + 1], v[32 * b + 4 * m + 2], v[32 * b + 4 * m + 3]);
+          fence_proxy_async_smem();
+          mbar_arrive(dqs_full);
+          if (warp == 10) {
+            if (!(ok = mbar_wait_warp(dqs_full, (qcnt - 1) & 1, status))) break;
+            if (lane == 0) {
+              for (int b = 0; b < 2; ++b)
+                tma_reduce_add_3d(&tm_dqacc, stage + b * (C::kDqStageBytes / 2), 32 * b, u.qtile(x) * kTileRows,
+                                  u.bh);
+              tma_store_commit();
+            }
+          }
+        }
         tr(42);
       }
       if (aborted(abort_flag)) ok = false;
     }
     if (!ok) *abort_flag = 1;
+    if (elected) tma_store_wait_all0();  // reductions in flight land before the CTA exits
   }
 
   tc_fence_before();
@@ -750,7 +880,8 @@ static cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
   auto kern = fa_bwd_main<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, a.lse2,
+  kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk,
+                                                       *a.tm_dv, a.lse2,
                                                        a.dsum,
                                                        a.dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dk),
                                                        reinterpret_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.Npad,

@@ -39,6 +39,7 @@ namespace fa {
 #define FA_FWD_POLY_EVERY 0
 #endif
 constexpr int kPolyEvery = FA_FWD_POLY_EVERY;
+constexpr int kPolyMod = kPolyEvery > 0 ? kPolyEvery : 1;  // divisor that is never zero
 
 #ifdef FA_TEST_HOOKS
 // Test builds only (-DFA_TEST_HOOKS, never the default library): when set,
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(320, 1)
             const int c = 32 * h + 2 * i;
             const uint64_t x = f2_fma(f2_pack(s[c], s[c + 1]), c2x2, negm);
             uint64_t p;
-            if (kPolyEvery > 0 && use_poly && (i % kPolyEvery) == kPolyEvery - 1) {
+            if (kPolyEvery > 0 && use_poly && (i % kPolyMod) == kPolyMod - 1) {
               p = ex2_poly2(x);
             } else {
               float x0, x1;

@@ -26,6 +26,8 @@ struct BwdLaunch {
   const CUtensorMap* tm_v;
   const CUtensorMap* tm_do;
   const CUtensorMap* tm_dqacc;  // fp32 [BH, N, d] accumulator, 32-column boxes (d = 64 path)
+  const CUtensorMap* tm_dk;     // bf16 [BH, N, d] outputs, 64-column boxes (stored with TMA at d = 64)
+  const CUtensorMap* tm_dv;
   const void* o;
   const void* dout;
   const float* lse;
