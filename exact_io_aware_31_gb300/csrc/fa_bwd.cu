@@ -15,31 +15,36 @@
 //                      0 and -inf), zero the fp32 dQ accumulator. (HBM-bound)
 //   2. fa_bwd_main     persistent; a unit is one 128-key tile of one (b, h);
 //                      K, V stay in shared memory while Q / dO tiles stream
-//                      past; dK, dV accumulate in TMEM; dQ partials are added
-//                      to the fp32 accumulator with vector reductions.
+//                      past; dK, dV accumulate in TMEM; each query tile's dQ
+//                      partial is added to the fp32 accumulator.
 //   3. fa_bwd_dq_conv  dQ = scale * accumulator -> bf16.       (HBM-bound)
 //
-// fa_bwd_main roles (10 warps):
-//   warps 0-7   two compute warpgroups, thread = key row, warpgroup g owning
-//               query columns [64 g, 64 g + 64): P^T = 2^(S^T c2 - lse2) ->
-//               TMEM (bf16, over its own S^T columns, for dV);
-//               dS^T = P^T (dP^T - D) -> shared memory (bf16, 128-byte
-//               swizzled, for dK and dQ); after P of tile i they also read
-//               half of tile i-1's dQ partial from TMEM (thread = query row),
-//               release it and reduce it into the fp32 accumulator (d = 64);
-//               their half of the dK/dV epilogue
-//   warp  8     TMA producer (K/V per unit, double-buffered at d = 64;
-//               Q, dO and their lse2 / D rows per query tile)
-//   warp  9     TMEM owner and MMA issuer
-//   warps 10-13 (d = 128) dQ warpgroup, thread = head-dimension index: reads
-//               each dQ^T partial, releases it, and issues its reductions
-// Tensor memory (512 columns): S^T [0,128) with P^T over [0,32) and
-// [64,96); dP^T [128,256); dV [256,256+d); dK [256+d, 256+2d); the dQ
-// partial in [384,448) at d = 64, and over dP^T at d = 128 (no columns left).
+// fa_bwd_main roles (n = FA_BWD_COMPUTE_WG compute warpgroups, default 4):
+//   warps 0 .. 4n-1   compute warpgroups, thread = key row, warpgroup g owning
+//                     query columns [g 128/n, (g+1) 128/n):
+//                     P^T = 2^(S^T c2 - lse2) -> TMEM (bf16, over the first
+//                     half of its own S^T columns, for dV);
+//                     dS^T = P^T (dP^T - D) -> shared memory (bf16, 128-byte
+//                     swizzled, for dK and dQ); at d = 128 they also drain
+//                     their columns of the previous tile's dQ^T partial with
+//                     coalesced reductions; their share of the dK/dV epilogue
+//   warp  4n          TMA producer (K/V per unit, double-buffered at d = 64;
+//                     Q, dO and their lse2 / D rows per query tile)
+//   warp  4n+1        TMEM owner and MMA issuer
+//   warps 4n+2 ..     (d = 64) dQ warpgroup, thread = query row: reads each dQ
+//                     partial, releases it, stages it in shared memory and
+//                     adds it with a tensor reduce-add
+// Tensor memory (512 columns): S^T [0,128); dP^T [128,256); dV [256,256+d);
+// dK [256+d, 256+2d); the dQ partial in [384,448) at d = 64, and over dP^T at
+// d = 128 (no columns left).
 // MMA issue order per query tile i:
-//   dP^T(i) | dV(i) S^T(i+1) | dK(i) dQ(i) | dP^T(i+1) ...
+//   d = 64:  dV(i) S^T(i+1) | dP^T(i+1) dK(i) dQ(i) | dV(i+1) ...
+//            (dP^T(i+1) as soon as dS(i) is in shared memory; dS is
+//            double-buffered, so dS(i+1) does not wait for dK(i), dQ(i))
+//   d = 128: dP^T(i) | dV(i) S^T(i+1) | dK(i) dQ^T(i) | dP^T(i+1) ...
+//            (dP^T(i+1) waits until dQ^T(i), in its columns, is drained)
 // so the compute warpgroups' dS(i) overlaps dV(i) and S^T(i+1), and their
-// P(i+1) overlaps dK(i), dQ(i) and dP^T(i+1).
+// P(i+1) overlaps the MMAs that follow dS(i).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -64,6 +69,17 @@ namespace fa {
 #define FA_BWD_POLY_EVERY 0
 #endif
 constexpr int kBwdPolyEvery = FA_BWD_POLY_EVERY;
+
+// Tuning knobs: compute warpgroups of the main kernel (2 or 4) at d = 64 and
+// d = 128; warpgroup g owns query columns [g 128/n, (g+1) 128/n) of every
+// tile.  More warpgroups hide more of the TMEM-load, MUFU and shared-memory
+// latency of the P and dS phases, at fewer registers per thread.
+#ifndef FA_BWD_COMPUTE_WG_D64
+#define FA_BWD_COMPUTE_WG_D64 2
+#endif
+#ifndef FA_BWD_COMPUTE_WG_D128
+#define FA_BWD_COMPUTE_WG_D128 4
+#endif
 constexpr int kBwdPolyMod = kBwdPolyEvery > 0 ? kBwdPolyEvery : 1;  // divisor that is never zero
 
 // ------------------------------------------------------------ preprocess ----
@@ -143,7 +159,7 @@ struct BwdCfg {
   static constexpr bool kDqTransposed = (D == 128);
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
-  // d = 64: a dedicated dQ warpgroup (warps 10-13) drains each partial
+  // d = 64: a dedicated dQ warpgroup (the last four warps) drains each partial
   // through the staging buffers with tensor reduce-adds (asynchronous, so it
   // never waits on them); d = 128: the compute warpgroups drain it with
   // coalesced reductions (FA_BWD_DQ_WARPGROUP selects the dedicated
@@ -153,9 +169,18 @@ struct BwdCfg {
   // MMAs are done) as two 64-column boxes with TMA stores; at d = 128 they
   // do not fit there and each thread stores its own row.
   static constexpr bool kEpiTma = (D == 64);
-  static constexpr int kThreads = kDqWarpgroup ? 448 : 320;
+  static constexpr int kWG = (D == 64) ? FA_BWD_COMPUTE_WG_D64 : FA_BWD_COMPUTE_WG_D128;  // compute warpgroups
+  static_assert(kWG == 2 || kWG == 4, "2 or 4 compute warpgroups");
+  static constexpr int kQCols = kTileRows / kWG;  // query columns per compute warpgroup
+  static constexpr int kDCols = D / kWG;          // dV / dK columns per compute warpgroup (epilogue)
+  static constexpr int kComputeWarps = 4 * kWG;
+  static constexpr int kComputeThreads = 32 * kComputeWarps;
+  static constexpr int kProducerWarp = kComputeWarps;
+  static constexpr int kMmaWarp = kComputeWarps + 1;
+  static constexpr int kDqWarp0 = kComputeWarps + 2;  // first warp of the dQ warpgroup
+  static constexpr int kThreads = 32 * (kComputeWarps + 2 + (kDqWarpgroup ? 4 : 0));
   static constexpr int kTmemCols = 512;
-  static constexpr int kColS = 0;     // S^T; P^T of query half g over columns [64 g, 64 g + 32)
+  static constexpr int kColS = 0;     // S^T; P^T of warpgroup g over columns [kQCols g, kQCols g + kQCols / 2)
   static constexpr int kColDP = 128;  // dP^T
   static constexpr int kColDV = 256;
   static constexpr int kColDK = 256 + D;
@@ -212,8 +237,13 @@ __device__ __forceinline__ BwdUnit bwd_decode(int pos, int nkt, bool causal) {
   return u;
 }
 
-// P^T column (32-bit, bf16 pairs) holding queries 16 k .. 16 k + 15.
-__device__ __forceinline__ uint32_t pt_col(int k) { return (k < 4) ? 8 * k : 64 + 8 * (k - 4); }
+// P^T column (32-bit, bf16 pairs) holding queries 16 k .. 16 k + 15: the
+// warpgroup owning them (QC query columns each) packs its P^T into the first
+// half of its own S^T columns.
+template <int QC>
+__device__ __forceinline__ uint32_t pt_col(int k) {
+  return QC * (k / (QC / 16)) + 8 * (k % (QC / 16));
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
@@ -245,7 +275,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   uint64_t* dkdv_full = s_full + 7;
   uint64_t* dkdv_empty = s_full + 8;
   uint64_t* mma_done = s_full + 9;
-  uint64_t* epi_full = s_full + 10;  // d = 64: dK / dV staged in the dS buffer (256 arrivals)
+  uint64_t* epi_full = s_full + 10;  // d = 64: dK / dV staged in the dS buffer (all compute threads)
   uint64_t* epi_free = s_full + 11;  // d = 64: their stores have read the dS buffer
   uint64_t* dqs_full = s_full + 12;  // d = 64: a dQ partial staged (128 arrivals)
   uint64_t* dqs_free = s_full + 13;  // d = 64: the staging buffer is free
@@ -270,24 +300,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_init(&qdo_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 256);
+    mbar_init(p_full, C::kComputeThreads);
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 256);
+    mbar_init(ds_full, C::kComputeThreads);
     mbar_init(ds_empty, 1);
     mbar_init(ds_empty2, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, C::kDqWarpgroup ? 128 : 256);
+    mbar_init(dq_empty, C::kDqWarpgroup ? 128 : C::kComputeThreads);
     mbar_init(dkdv_full, 1);
-    mbar_init(dkdv_empty, 256);
+    mbar_init(dkdv_empty, C::kComputeThreads);
     mbar_init(mma_done, 1);
-    mbar_init(epi_full, 256);
+    mbar_init(epi_full, C::kComputeThreads);
     mbar_init(epi_free, 1);
     mbar_init(dqs_full, 128);
     mbar_init(dqs_free, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
@@ -296,7 +326,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       Tracer tr(3);
@@ -390,7 +420,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_wait(&do_full[x % C::kStages], (x / C::kStages) & 1, status);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T: both K-major over d
@@ -469,7 +499,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ts(tbase + C::kColDV, tbase + C::kColS + pt_col(k),
+            mma_ts(tbase + C::kColDV, tbase + C::kColS + pt_col<C::kQCols>(k),
                    sdesc(do_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
           tr(19);
           // S^T(i+1) as early as possible
@@ -529,20 +559,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mma_commit(mma_done);
       mbar_wait(mma_done, 0, status);
     }
-  } else if (warp < 8) {
+  } else if (warp < C::kComputeWarps) {
     // ------------------------------------------------ compute warpgroups --
-    // Warpgroup g owns query columns [64 g, 64 g + 64) of P^T / dS^T and
-    // columns [g d/2, (g+1) d/2) of the dQ partial, dV and dK.
+    // Warpgroup g owns query columns [kQCols g, kQCols (g+1)) of P^T / dS^T
+    // (and of the dQ^T partial at d = 128), and columns [kDCols g,
+    // kDCols (g+1)) of dV and dK.
+    constexpr int kQC = C::kQCols;
+    constexpr int kDC = C::kDCols;
     const int g = warp / 4;
     const int quarter = warp % 4;
-    const int r = quarter * 32 + lane;  // key row (P, dS, dK, dV) / query row (dQ) within the tile
+    const int r = quarter * 32 + lane;  // key row (P, dS, dK, dV) / head-dimension row (dQ^T) in the tile
     const uint32_t lanes = (uint32_t)quarter * 32;
-    const uint32_t t_s = tmem_lane_col(tbase, lanes, C::kColS + 64 * g);
-    const uint32_t t_dp = tmem_lane_col(tbase, lanes, C::kColDP + 64 * g);
-    const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + (C::kDqTransposed ? 64 : D / 2) * g);
-    const uint32_t t_dv = tmem_lane_col(tbase, lanes, C::kColDV + (D / 2) * g);
-    const uint32_t t_dk = tmem_lane_col(tbase, lanes, C::kColDK + (D / 2) * g);
-    uint8_t* ds_row0 = sm + C::kOffDS + g * kSwzBlockBytes + r * 128;  // + buffer * kDsBytes
+    const uint32_t t_s = tmem_lane_col(tbase, lanes, C::kColS + kQC * g);
+    const uint32_t t_dp = tmem_lane_col(tbase, lanes, C::kColDP + kQC * g);
+    const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + kQC * g);
+    const uint32_t t_dv = tmem_lane_col(tbase, lanes, C::kColDV + kDC * g);
+    const uint32_t t_dk = tmem_lane_col(tbase, lanes, C::kColDK + kDC * g);
+    // dS^T row r in shared memory: query q is 16-byte chunk q / 8 of the row,
+    // in swizzle block (q / 8) / 8 at position (q / 8) % 8.
+    const int chunk0 = kQC * g / 8;
+    uint8_t* ds_row0 = sm + C::kOffDS + (chunk0 / 8) * kSwzBlockBytes + r * 128;  // + buffer * kDsBytes
+    const int cbase = chunk0 % 8;
     const int swz = r & 7;
     const uint64_t c2x2 = f2_pack(c2, c2);
     uint32_t scnt = 0, dpcnt = 0, dse = 0, ucnt = 0, qit = 0, dqcnt = 0;
@@ -561,20 +598,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ++dqcnt;
       tc_fence_after();
       if (C::kDqTransposed) {
-        // lane = head-dimension index r, columns = queries 64 g .. 64 g + 63:
+        // lane = head-dimension index r, columns = this warpgroup's queries:
         // one scalar reduction per query, 128 contiguous bytes per warp.
-        uint32_t v[64];
-        tmem_ld32(t_dq, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(t_dq + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        uint32_t v[kQC];
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c) tmem_ld32(t_dq + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(dq_empty);
         tr(41);
-        const int q0 = qt * kTileRows + 64 * g;
+        const int q0 = qt * kTileRows + kQC * g;
         float* dst = dq_acc + ((size_t)bh * N + q0) * D + r;
         const int nvalid = N - q0;
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kQC; ++c)
           if (c < nvalid) red_add(dst + (size_t)c * D, __uint_as_float(v[c]));
       }
       return true;
@@ -589,12 +626,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const bool key_ok = kr < N;
       for (int x = 0; x < u.nq; ++x, ++qit) {
         const int i = u.qtile(x);
-        const int qbase = i * kTileRows + 64 * g;  // first query of this warpgroup's columns
+        const int qbase = i * kTileRows + kQC * g;  // first query of this warpgroup's columns
         const bool diag = CAUSAL && (i == u.j);
         const bool full_tile = (i + 1) * kTileRows <= N;  // no padded queries (their P must stay exactly 0)
         // -lse2 / -D of this query tile, staged in shared memory with Q / dO
         const float* rows =
-            reinterpret_cast<const float*>(sm + C::kOffRow + (qit % C::kStages) * C::kRowBytes) + 64 * g;
+            reinterpret_cast<const float*>(sm + C::kOffRow + (qit % C::kStages) * C::kRowBytes) + kQC * g;
         // ---- P^T = 2^(S^T c2 - lse2); masked entries exactly 0 ----
         tr(1);
         ok = mbar_wait_warp(s_full, scnt & 1, status);
@@ -602,9 +639,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         ++scnt;
         if (!ok) break;
         tc_fence_after();
-        uint32_t pk[32];  // P^T row half, bf16 pairs (reused for dS)
+        uint32_t pk[kQC / 2];  // this warpgroup's P^T row, bf16 pairs (reused for dS)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kQC / 32; ++c) {
           uint32_t sv[32];
           tmem_ld32(t_s + 32 * c, sv);
           tmem_wait_ld();
@@ -629,9 +666,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             pk[16 * c + e] = key_ok ? pack_bf16x2(p0, p1) : 0u;
           }
         }
-        // S^T of this half is fully read: P^T goes over its first 32 columns.
-        tmem_st16(t_s, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(t_s + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        // This warpgroup's S^T columns are fully read: P^T goes over the first half.
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c) tmem_st16(t_s + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_full);
@@ -668,7 +705,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kQC / 32; ++c) {
           uint32_t dpv[32];
           tmem_ld32(t_dp + 32 * c, dpv);
           tmem_wait_ld();
@@ -687,7 +724,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               f2_unpack(f2_mul(f2_pack(pf.x, pf.y), t), d0, d1);
               dsk[e] = pack_bf16x2(d0, d1);
             }
-            *reinterpret_cast<uint4*>(ds_row + ((m ^ swz) * 16)) = make_uint4(dsk[0], dsk[1], dsk[2], dsk[3]);
+            *reinterpret_cast<uint4*>(ds_row + (((cbase + m) ^ swz) * 16)) = make_uint4(dsk[0], dsk[1], dsk[2], dsk[3]);
           }
         }
         fence_proxy_async_smem();
@@ -710,19 +747,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (C::kEpiTma) {
         // dV, dK (x scale) -> bf16 in the dS buffer as 128-byte-swizzled
         // 64-column boxes (block 0 dV, block 1 dK; this warpgroup writes
-        // columns [32 g, 32 g + 32) of its key row), then one thread stores
-        // both boxes.  Rows past N are clipped by the copy.
-        uint32_t a[32], b[32];
-        tmem_ld32(t_dv, a);
-        tmem_ld32(t_dk, b);
+        // columns [kDCols g, kDCols (g+1)) of its key row), then one thread
+        // stores both boxes.  Rows past N are clipped by the copy.
+        uint32_t a[kDC], b[kDC];
+#pragma unroll
+        for (int c = 0; c < kDC / 16; ++c) {
+          tmem_ld16(t_dv + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&a[16 * c]));
+          tmem_ld16(t_dk + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&b[16 * c]));
+        }
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(dkdv_empty);  // the next unit may overwrite the columns
         uint8_t* rv = sm + C::kOffDS + r * 128;
         uint8_t* rk = rv + kSwzBlockBytes;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int ch = ((4 * g + m) ^ swz) * 16;
+        for (int m = 0; m < kDC / 8; ++m) {
+          const int ch = ((kDC * g / 8 + m) ^ swz) * 16;
           *reinterpret_cast<uint4*>(rv + ch) =
               make_uint4(pack_bf16x2(__uint_as_float(a[8 * m]), __uint_as_float(a[8 * m + 1])),
                          pack_bf16x2(__uint_as_float(a[8 * m + 2]), __uint_as_float(a[8 * m + 3])),
@@ -748,14 +788,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         epi_pending = true;
         if (!ok) break;
       } else {
-        const size_t rowoff = ((size_t)u.bh * N + kr) * D + (D / 2) * g;
+        // Each thread stores its key row's kDCols columns of dV and dK.
+        const size_t rowoff = ((size_t)u.bh * N + kr) * D + kDC * g;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < kDC / 32; ++c) {
           uint32_t a[32], b[32];
           tmem_ld32(t_dv + 32 * c, a);
           tmem_ld32(t_dk + 32 * c, b);
           tmem_wait_ld();
-          if (c == D / 64 - 1) {  // dK / dV columns read: the next unit may overwrite them
+          if (c == kDC / 32 - 1) {  // dK / dV columns read: the next unit may overwrite them
             tc_fence_before();
             mbar_arrive(dkdv_empty);
           }
@@ -795,10 +836,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;
     const uint32_t t_dq = tmem_lane_col(tbase, quarter * 32, C::kColDQ);
-    const bool elected = (warp == 10) && (lane == 0);
+    const bool elected = (warp == C::kDqWarp0) && (lane == 0);
     uint32_t qcnt = 0;
     bool ok = true;
-    Tracer tr(warp == 12 ? 1 : -1);
+    Tracer tr(warp == C::kDqWarp0 + 2 ? 1 : -1);
     for (int round = 0; ok; ++round) {
       if (round * grid >= total_units) break;
       const int pos = snake_unit(round, blockIdx.x, grid);
@@ -831,23 +872,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             mbar_arrive(dqs_free);
           }
           if (!(ok = mbar_wait_warp(dqs_free, (qcnt - 1) & 1, status))) break;
-          uint32_t v[64];
-          tmem_ld32(t_dq, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(t_dq + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(dq_empty);
-          tr(41);
+          // Both 32-column halves at once; with 4 compute warpgroups (fewer
+          // registers per thread) one half at a time.
+          constexpr int kHalvesAtOnce = (C::kWG == 4) ? 1 : 2;
           const int swz = r & 7;
 #pragma unroll
-          for (int b = 0; b < 2; ++b)
+          for (int b0 = 0; b0 < 2; b0 += kHalvesAtOnce) {
+            uint32_t v[32 * kHalvesAtOnce];
 #pragma unroll
-            for (int m = 0; m < 8; ++m)
-              *reinterpret_cast<uint4*>(stage + b * (C::kDqStageBytes / 2) + r * 128 + ((m ^ swz) * 16)) =
-                  make_uint4(v[32 * b + 4 * m], v[32 * b + 4 * m + 1], v[32 * b + 4 * m + 2], v[32 * b + 4 * m + 3]);
+            for (int h = 0; h < kHalvesAtOnce; ++h)
+              tmem_ld32(t_dq + 32 * (b0 + h), *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+            tmem_wait_ld();
+            if (b0 + kHalvesAtOnce == 2) {  // the whole row is read: release the columns
+              tc_fence_before();
+              mbar_arrive(dq_empty);
+              tr(41);
+            }
+#pragma unroll
+            for (int h = 0; h < kHalvesAtOnce; ++h)
+#pragma unroll
+              for (int m = 0; m < 8; ++m)
+                *reinterpret_cast<uint4*>(stage + (b0 + h) * (C::kDqStageBytes / 2) + r * 128 + ((m ^ swz) * 16)) =
+                    make_uint4(v[32 * h + 4 * m], v[32 * h + 4 * m + 1], v[32 * h + 4 * m + 2],
+                               v[32 * h + 4 * m + 3]);
+          }
           fence_proxy_async_smem();
           mbar_arrive(dqs_full);
-          if (warp == 10) {
+          if (warp == C::kDqWarp0) {
             if (!(ok = mbar_wait_warp(dqs_full, (qcnt - 1) & 1, status))) break;
             if (lane == 0) {
               for (int b = 0; b < 2; ++b)
@@ -867,7 +918,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, C::kTmemCols);
@@ -882,8 +933,7 @@ static cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk,
                                                        *a.tm_dv, a.lse2,
-                                                       a.dsum,
-                                                       a.dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dk),
+                                                       a.dsum, a.dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dk),
                                                        reinterpret_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.Npad,
                                                        a.c2, a.scale, a.status);
   return cudaGetLastError();

@@ -89,3 +89,36 @@ def test_zero_scale_is_uniform_attention(causal):
     grads = run_bwd(qg, kg, vg, o, lse, do, 0.0, causal)
     _, _, g_ref = _oracle_case(q, k, v, do, 0.0, causal)
     assert_grads_close(grads, g_ref, "scale=0")
+
+
+SPLIT = [(2, 2, 300, 64, True), (1, 3, 513, 64, False), (1, 2, 300, 128, True), (2, 1, 257, 128, False)]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", SPLIT, ids=[f"b{b}h{h}n{n}d{d}{'c' if c else ''}" for b, h, n, d, c in SPLIT])
+def test_split_phases_match_oracle(B, H, N, d, causal):
+    """fa_bwd_preprocess -> fa_bwd_dkdv -> fa_bwd_dq_convert on one workspace.
+
+    The workspace starts as garbage (0xAB bytes): the preprocess must reset the
+    dQ accumulator.  Run twice on the same workspace, so a finished call's
+    accumulator is reset too.
+    """
+    import torch
+
+    import exact_io_aware_31_gb300 as fa
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = make_inputs(B, H, N, d, seed=4100 + N + d + causal)
+    qg, kg, vg, o, lse = run_fwd(q, k, v, scale, causal)
+    dog = do.cuda()
+    nbytes = fa.fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.full((nbytes,), 0xAB, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    _, _, g_ref = _oracle_case(q, k, v, do, scale, causal)
+    for rep in range(2):
+        dq, dk, dv = (torch.full_like(qg, float("nan")) for _ in range(3))
+        assert fa.fa_bwd_preprocess(o.data_ptr(), dog.data_ptr(), lse.data_ptr(), B, H, N, d, ws.data_ptr(), nbytes,
+                                    s) == fa.FA_OK
+        assert fa.fa_bwd_dkdv(qg.data_ptr(), kg.data_ptr(), vg.data_ptr(), dog.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, N, d, scale, int(causal), ws.data_ptr(), nbytes, s) == fa.FA_OK
+        assert fa.fa_bwd_dq_convert(dq.data_ptr(), B, H, N, d, scale, ws.data_ptr(), nbytes, s) == fa.FA_OK
+        assert fa.fa_get_device_status(s) == fa.FA_OK
+        assert_grads_close((dq, dk, dv), g_ref, f"split {(B, H, N, d, causal)} rep {rep}")
