@@ -84,9 +84,20 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def source_hash():
+# The device code of each profiled kernel: its translation unit and the device
+# headers it includes (host-side launch plumbing is not part of it).
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["fa_fwd.cu"],
+    "fa_bwd_pre": ["fa_bwd.cu"],
+    "fa_bwd_main": ["fa_bwd.cu"],
+    "fa_bwd_dq_conv": ["fa_bwd.cu"],
+}
+DEVICE_HEADERS = ["fa_common.cuh", "sm103_ptx.cuh", "exp2_poly.h"]
+
+
+def source_hash(kernel):
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in KERNEL_SOURCES[kernel] + DEVICE_HEADERS:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -100,7 +111,7 @@ def dram_traffic(kernel, workload):
     with open(path) as f:
         table = json.load(f)
     rec = table.get(kernel, {}).get(workload)
-    if not rec or rec.get("source_sha") != source_hash():
+    if not rec or kernel not in KERNEL_SOURCES or rec.get("source_sha") != source_hash(kernel):
         return None
     return rec.get("bytes_per_launch")
 
