@@ -412,6 +412,129 @@ def run_ours(args, w):
         torch.distributed.destroy_process_group()
 
 
+DECODE_METRIC = "split-KV decode forward: K/V cache read GB/s (1 GPU)"
+
+
+def decode_bytes(w):
+    """Algorithmic HBM bytes of one decode step: read Q, K, V; write O and lse."""
+    return 2 * w.B * w.H * w.Nk * w.d * 2 + 2 * w.B * w.H * w.Nq * w.d * 2 + 4 * w.B * w.H * w.Nq
+
+
+def run_decode(args, w):
+    """Split-KV decode forward (fa_fwd_splitkv): device-timed GB/s against the HBM roofline."""
+    import exact_io_aware_31_gb300 as fa
+    from exact_io_aware_31_gb300 import build
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    build.build()
+    fa.load_library()
+    q, k, v = workloads.make_decode_inputs(w.B, w.H, w.Nq, w.Nk, w.d, w.seed)
+    dev = torch.device("cuda", local)
+    qg, kg, vg = (t.to(dev) for t in (q, k, v))
+    o = torch.empty_like(qg)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    splits = 0
+    ws_bytes = fa.fa_fwd_splitkv_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d, splits)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        st = fa.fa_fwd_splitkv(qg.data_ptr(), kg.data_ptr(), vg.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H,
+                               w.Nq, w.Nk, w.d, w.scale, int(w.causal), splits, ws.data_ptr(), ws_bytes, sh)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd_splitkv")
+
+    for _ in range(args.warmup):
+        step()
+        flush_buf.zero_()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_busy = time.perf_counter()
+    busy = 0
+    while time.perf_counter() - t_busy < 0.6:
+        step()
+        busy += 1
+        if busy % 32 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in events:
+        flush_buf.zero_()   # the cache is about L2-sized: every timed step reads it from HBM
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if clocks is not None:
+        clocks["window"] = f"{busy} untimed identical steps, then the timed region"
+    if fa.fa_get_device_status(sh) != fa.FA_OK:
+        raise RuntimeError("device status after the timed region")
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in events)
+    nbytes = decode_bytes(w)
+    value = nbytes / (ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    # splits per head under the automatic choice (the library's rule: one CTA per SM, at most one per tile)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nsplit = min((w.Nk + 127) // 128, max(1, sms // (w.B * w.H)))
+    # ---- end to end: the cache and queries from pinned host memory, results back ----
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for hd, dd in ((hq, qg), (hk, kg), (hv, vg)):
+            dd.copy_(hd, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 10))
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * 2 + hlse.numel() * 4
+    launches = 1 if ws_bytes == 0 else 2
+    line = {"metric": DECODE_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
+            "config": {**w.describe(), "parallelism": "single GPU", "splits_per_head": int(nsplit),
+                       "l2": "flushed before every timed step (2x L2 buffer written)",
+                       "bytes_per_step": nbytes},
+            "roofline": {"kernel": "fa_decode_split (+ fa_decode_combine)", "bound": "hbm",
+                         "achieved": round(value, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(value / peaks["hbm_gbs"], 4), "traffic": None, "peak_source": peak_src},
+            "gpu_launches": launches * args.steps, "clocks": clocks,
+            "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps}}
+    if not args.no_cpu_baseline:
+        import numpy as np
+        from oracle.decode import attention_forward_rect
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < args.cpu_seconds and n < w.B * w.H:
+            b, h = divmod(n, w.H)
+            attention_forward_rect(*(t[b:b + 1, h:h + 1].double().numpy() for t in (q, k, v)), w.scale, w.causal)
+            n += 1
+        el = time.perf_counter() - t0
+        cpu_gbs = nbytes * n / (w.B * w.H) / el / 1e9
+        line["cpu_baseline"] = {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cores(), "kind": "oracle",
+                                "sample": f"{n} of {w.B * w.H} heads in fp64 numpy, {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,7 +542,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.GPT2_MEDIUM.name,
-                    help="one of: " + ", ".join(sorted(workloads.BY_NAME)))
+                    help="one of: " + ", ".join(sorted(workloads.BY_NAME) + sorted(workloads.DECODE_BY_NAME)))
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
     ap.add_argument("--ref-seconds", type=float, default=None,
                     help="oracle time per step for --impl reference (default: 150 s spread over all steps)")
@@ -429,6 +552,13 @@ def main():
         args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.ref_seconds is None:
         args.ref_seconds = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    if args.workload in workloads.DECODE_BY_NAME:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the forward/backward "
+                              "workloads; the decode row reports its oracle under cpu_baseline"}))
+            return
+        run_decode(args, workloads.DECODE_BY_NAME[args.workload])
+        return
     w = workloads.BY_NAME[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -8,8 +8,10 @@ or the device is not sm_103, calls raise.
 Raw entry points (same names and argument order as the C ABI, pointers as
 ints):  ``fa_fwd``, ``fa_bwd``, ``fa_bwd_workspace_size``, the three phases
 of ``fa_bwd`` (``fa_bwd_preprocess``, ``fa_bwd_dkdv``, ``fa_bwd_dq_convert``),
-``fa_get_device_status``, ``fa_status_string``.
-Tensor helpers: :func:`forward`, :func:`backward`.
+the split-KV decode forward (``fa_fwd_splitkv``,
+``fa_fwd_splitkv_workspace_size``), ``fa_get_device_status``,
+``fa_status_string``.
+Tensor helpers: :func:`forward`, :func:`backward`, :func:`decode_forward`.
 """
 
 from __future__ import annotations
@@ -20,6 +22,7 @@ import os
 __all__ = [
     "LIB_PATH", "FaError", "load_library", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "decode_forward",
     "fa_get_device_status", "fa_status_string", "forward", "backward", "EXPORTED_SYMBOLS",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_WORKSPACE", "FA_ERR_CUDA",
     "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_INTERNAL",
@@ -36,7 +39,8 @@ FA_ERR_DEVICE_TIMEOUT = 5
 FA_ERR_INTERNAL = 6
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_dkdv",
-                    "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_get_device_status", "fa_status_string")
+                    "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
+                    "fa_get_device_status", "fa_status_string")
 
 # Size of the library-owned scratch behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -75,6 +79,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_dq_convert.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
+    lib.fa_fwd_splitkv_workspace_size.restype = sz
+    lib.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.fa_get_device_status.restype = i
     lib.fa_get_device_status.argtypes = [vp]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -114,6 +122,16 @@ def fa_bwd_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream)
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, stream) -> int:
     """fa_bwd with the library's own scratch instead of a workspace (for callers that cannot allocate)."""
     return load_library().fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, stream)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, workspace, workspace_bytes,
+                   stream) -> int:
+    return load_library().fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, workspace,
+                                         workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits) -> int:
+    return load_library().fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits)
 
 
 def fa_get_device_status(stream) -> int:
@@ -182,3 +200,31 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, gr
     if st != FA_OK:
         raise FaError(st, "fa_bwd")
     return dq, dk, dv
+
+
+def decode_forward(q, k, v, scale=None, causal=True, num_splits=0, out=None, lse=None, workspace=None,
+                   stream=None):
+    """Split-KV attention of ``q [B, H, Nq, d]`` (Nq <= 8, the last Nq positions) against the cache
+    ``k, v [B, H, Nk, d]`` (bf16 CUDA tensors); returns ``(o, lse)``."""
+    import torch
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    _check(q, "q", (B, H, Nq, d), torch.bfloat16)
+    for name, t in (("k", k), ("v", v)):
+        _check(t, name, (B, H, Nk, d), torch.bfloat16)
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(o, "out", (B, H, Nq, d), torch.bfloat16)
+    _check(l, "lse", (B, H, Nq), torch.float32)
+    need = fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wptr = workspace.data_ptr() if workspace is not None else None
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, Nq, Nk, d,
+                        float(scale), int(bool(causal)), int(num_splits), wptr, wbytes, _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_splitkv")
+    return o, l

@@ -181,6 +181,89 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   return FA_OK;
 }
 
+namespace fa {
+namespace {
+
+constexpr int kMaxDecodeQueries = 8;
+
+int check_decode(int B, int H, int Nq, int Nk, int d, float scale, int causal, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  if (bh > INT_MAX || (long long)Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
+  const long long kpad = ((long long)Nk + 127) / 128 * 128;
+  if (bh * kpad * (d > 0 ? d : 1) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;  // a query would see no key
+  if (Nq > kMaxDecodeQueries) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// Splits actually used: the requested number, or (0) as many as fill the SMs
+// with one CTA each; never more than the 128-key tiles of the cache.
+int decode_splits(long long bh, int Nk, int num_splits, int sms) {
+  const int tiles = (Nk + 127) / 128;
+  long long s = num_splits > 0 ? num_splits : (sms / bh > 1 ? sms / bh : 1);
+  if (s > tiles) s = tiles;
+  return (int)s;
+}
+
+size_t decode_partials_bytes(long long bh, int Nq, int d, int splits) {
+  if (splits <= 1) return 0;
+  return round256((size_t)splits * bh * Nq * d * 4) + round256((size_t)splits * bh * Nq * 4);
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (check_decode(B, H, Nq, Nk, d, 1.0f, 0, num_splits) != FA_OK) return 0;
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != FA_OK) return 0;
+  const long long bh = (long long)B * H;
+  return decode_partials_bytes(bh, Nq, d, decode_splits(bh, Nk, num_splits, dev->sms));
+}
+
+extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                              int Nk, int d, float scale, int causal, int num_splits, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  int st = check_decode(B, H, Nq, Nk, d, scale, causal, num_splits);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const int BH = B * H;
+  DecLaunch a;
+  a.splits = decode_splits(BH, Nk, num_splits, dev->sms);
+  const size_t need = decode_partials_bytes(BH, Nq, d, a.splits);
+  if (need > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                   workspace_bytes < need))
+    return FA_ERR_WORKSPACE;
+  CUtensorMap tk, tv;
+  if (make_map(&tk, k, BH, Nk, d) || make_map(&tv, v, BH, Nk, d)) return FA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.tm_k = &tk;
+  a.tm_v = &tv;
+  a.q = q;
+  a.o = o;
+  a.lse = lse;
+  a.part_o = need ? reinterpret_cast<float*>(ws) : nullptr;
+  a.part_lse2 = need ? reinterpret_cast<float*>(ws + round256((size_t)a.splits * BH * Nq * d * 4)) : nullptr;
+  a.BH = BH;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.causal = causal;
+  a.c2 = log2_scale(scale);
+  a.status = dev->status;
+  if (launch_decode(a, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_sizes(B, H, N, d, 1.0f, 0) != FA_OK) return 0;
   return workspace_layout(B, H, N, d).total;

@@ -1,0 +1,360 @@
+// Split-KV forward for decoding: a few new queries against a long key/value
+// cache.
+//
+// lensaml.com "FlashAttention" FAQ "Does FlashAttention help during LLM
+// decoding?": each decode step has one query (or a few) per sequence, so the
+// score matrix is a row and the cost is reading the cache; Flash-Decoding
+// splits that read over many thread blocks.  Here a split is a run of whole
+// 128-key tiles of one (b, h); its CTA streams the K/V tiles (TMA, 128-byte
+// swizzled boxes, a ring of stages) and keeps the online-softmax state of
+// every query of the head (blog.teqners.com, "Softmax is the anti-tiling
+// operation" and "FlashAttention's move: rescale the output, too").  With one
+// split per head the CTA writes O and lse itself; otherwise each split writes
+// its normalised partial output and base-2 logsumexp, and a second kernel
+// merges them with the same rescale rule.
+//
+// At 1-8 queries the work is 4 Nq d FLOPs per key against 4 d bytes of K and
+// V, at most 8 FLOP/B: far below the tensor-core ridge, so the contractions
+// run on the CUDA cores in fp32 and the kernel is bound by HBM.
+//
+// fa_decode_split (128 threads, one CTA per (b, h, split)):
+//   scores  thread = key of the tile: s_n = c2 * q_n . k over 16-byte chunks
+//           of the swizzled K row (queries in shared memory, read as
+//           broadcasts); masked keys -inf.
+//   softmax per query, across the CTA: tile max, rescale factor, p = 2^(s - m)
+//           into shared memory, tile sum.
+//   PV      thread = column pair x key group: acc_n += p_n(key) * v(key) over
+//           the keys of its group; groups are summed at the end.
+// fa_decode_combine: one warp per (b, h, query) merges the splits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_common.cuh"
+#include "fa_kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct DecCfg {
+  static constexpr int kTileKeys = kTileRows;            // 128 keys per tile
+  static constexpr int kTileBytes = kTileKeys * D * 2;   // one K or V tile: D / 64 swizzle blocks
+  static constexpr int kBlocks = D / 64;
+  static constexpr int kStages = (D == 64) ? 4 : 3;      // K+V stages in flight
+  static constexpr int kThreads = 128;
+  static constexpr int kPairs = D / 2;                   // column pairs (PV phase)
+  static constexpr int kGroups = kThreads / kPairs;      // key groups (PV phase): 2 at d = 128, 4 at d = 64
+  static constexpr int kOffK = 0;                                  // [stages] K tiles
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;       // [stages] V tiles
+  static constexpr int kOffQ = kOffV + kStages * kTileBytes;       // [8][D] fp32 queries
+  static constexpr int kOffP = kOffQ + 8 * D * 4;                  // [128 keys][8] fp32 probabilities
+  static constexpr int kOffRed = kOffP + kTileKeys * 8 * 4;        // [2][4 warps][8] fp32 reductions
+  static constexpr int kOffAcc = kOffRed + 2 * 4 * 8 * 4;          // [groups][8][D] fp32 partial outputs
+  static constexpr int kOffBar = kOffAcc + kGroups * 8 * D * 4;    // [stages] mbarriers
+  static constexpr int kOffAbort = kOffBar + 8 * kStages;
+  static constexpr int kSmemBytes = kOffAbort + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kGroups * kPairs == kThreads, "PV mapping");
+};
+
+// NQ: queries handled (Nq rounded up to 1, 2, 4 or 8; slots past Nq stay masked).
+template <int D, int NQ, bool CAUSAL>
+__global__ void __launch_bounds__(128, 1)
+    fa_decode_split(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                    float* __restrict__ part_o, float* __restrict__ part_lse2, int BH, int Nq, int Nk, int splits,
+                    float c2, int* status) {
+  using C = DecCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (!smem_base_ok(smem_raw, status)) return;
+  uint8_t* sm = smem_raw;
+  float* qs = reinterpret_cast<float*>(sm + C::kOffQ);
+  float* ps = reinterpret_cast<float*>(sm + C::kOffP);
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);
+  float* accs = reinterpret_cast<float*>(sm + C::kOffAcc);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
+
+  const int tid = threadIdx.x;
+  const int warp = tid / 32, lane = tid % 32;
+  const int bh = blockIdx.x / splits;
+  const int split = blockIdx.x - bh * splits;
+  const int tiles = (Nk + kTileRows - 1) / kTileRows;
+  const int t0 = (int)((long long)split * tiles / splits);
+  const int t1 = (int)((long long)(split + 1) * tiles / splits);
+  const int kend = min(t1 * kTileRows, Nk);
+  const int shift = Nk - Nq;  // bottom-right causal: key j visible to query n iff j <= n + shift
+
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) mbar_init(&full[s], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // Queries -> fp32 in shared memory (slots past Nq are zero and stay masked).
+  for (int i = tid; i < NQ * D; i += C::kThreads) {
+    const int n = i / D;
+    qs[i] = (n < Nq) ? __bfloat162float(q[((size_t)bh * Nq + n) * D + (i - n * D)]) : 0.f;
+  }
+  __syncthreads();
+  auto issue = [&](int it) {  // tile it into its stage
+    const int st = (it - t0) % C::kStages;
+    mbar_expect_tx(&full[st], 2 * C::kTileBytes);
+    for (int b = 0; b < C::kBlocks; ++b) {
+      tma_load_3d(sm + C::kOffK + st * C::kTileBytes + b * kSwzBlockBytes, &tm_k, &full[st], 64 * b,
+                  it * kTileRows, bh);
+      tma_load_3d(sm + C::kOffV + st * C::kTileBytes + b * kSwzBlockBytes, &tm_v, &full[st], 64 * b,
+                  it * kTileRows, bh);
+    }
+  };
+  if (tid == 0) {
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+    for (int it = t0; it < t1 && it < t0 + C::kStages; ++it) issue(it);
+  }
+
+  float m_run[NQ], l_run[NQ];  // log2 units; the same in every thread
+#pragma unroll
+  for (int n = 0; n < NQ; ++n) {
+    m_run[n] = -INFINITY;
+    l_run[n] = 0.f;
+  }
+  const int cp = tid % C::kPairs;  // PV phase: columns 2 cp, 2 cp + 1
+  const int kg = tid / C::kPairs;  // PV phase: keys kg, kg + kGroups, ...
+  float acc[NQ][2];
+#pragma unroll
+  for (int n = 0; n < NQ; ++n) acc[n][0] = acc[n][1] = 0.f;
+  const int swz = tid & 7;
+
+  int issued = min(t1, t0 + C::kStages);
+  for (int it = t0; it < t1; ++it) {
+    const int st = (it - t0) % C::kStages;
+    if (!mbar_wait(&full[st], ((it - t0) / C::kStages) & 1, status)) *abort_flag = 1;
+    __syncthreads();
+    if (*abort_flag) break;
+    const uint8_t* ks = sm + C::kOffK + st * C::kTileBytes;
+    const uint8_t* vs = sm + C::kOffV + st * C::kTileBytes;
+
+    // ---- scores: thread = key ----
+    const int key = it * kTileRows + tid;
+    float sc[NQ];
+#pragma unroll
+    for (int n = 0; n < NQ; ++n) sc[n] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 kv = *reinterpret_cast<const uint4*>(ks + (c / 8) * kSwzBlockBytes + tid * 128 +
+                                                       (((c % 8) ^ swz) * 16));
+      const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&kv);
+      float kf[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(kp[e]);
+        kf[2 * e] = f.x;
+        kf[2 * e + 1] = f.y;
+      }
+#pragma unroll
+      for (int n = 0; n < NQ; ++n) {
+        const float4 qa = *reinterpret_cast<const float4*>(qs + n * D + 8 * c);
+        const float4 qb = *reinterpret_cast<const float4*>(qs + n * D + 8 * c + 4);
+        sc[n] = fmaf(qa.x, kf[0], sc[n]);
+        sc[n] = fmaf(qa.y, kf[1], sc[n]);
+        sc[n] = fmaf(qa.z, kf[2], sc[n]);
+        sc[n] = fmaf(qa.w, kf[3], sc[n]);
+        sc[n] = fmaf(qb.x, kf[4], sc[n]);
+        sc[n] = fmaf(qb.y, kf[5], sc[n]);
+        sc[n] = fmaf(qb.z, kf[6], sc[n]);
+        sc[n] = fmaf(qb.w, kf[7], sc[n]);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < NQ; ++n) {
+      const bool vis = n < Nq && key < kend && (!CAUSAL || key <= n + shift);
+      sc[n] = vis ? sc[n] * c2 : -INFINITY;
+    }
+    // ---- tile maximum per query, across the CTA ----
+#pragma unroll
+    for (int n = 0; n < NQ; ++n) {
+      float mx = sc[n];
+#pragma unroll
+      for (int off = 16; off > 0; off /= 2) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if (lane == 0) red[warp * 8 + n] = mx;
+    }
+    __syncthreads();
+    float m_new[NQ], alpha[NQ];
+#pragma unroll
+    for (int n = 0; n < NQ; ++n) {
+      const float mt = fmaxf(fmaxf(red[n], red[8 + n]), fmaxf(red[16 + n], red[24 + n]));
+      m_new[n] = fmaxf(m_run[n], mt);
+      alpha[n] = (m_run[n] == m_new[n]) ? 1.f : ex2(m_run[n] - m_new[n]);  // 0 when m_run = -inf
+      const float p = (sc[n] == -INFINITY) ? 0.f : ex2(sc[n] - m_new[n]);
+      ps[tid * 8 + n] = p;
+      float sum = p;
+#pragma unroll
+      for (int off = 16; off > 0; off /= 2) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (lane == 0) red[32 + warp * 8 + n] = sum;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int n = 0; n < NQ; ++n) {
+      const float lt = (red[32 + n] + red[40 + n]) + (red[48 + n] + red[56 + n]);
+      l_run[n] = alpha[n] * l_run[n] + lt;
+      m_run[n] = m_new[n];
+      acc[n][0] *= alpha[n];
+      acc[n][1] *= alpha[n];
+    }
+    // ---- O += P V: thread = column pair cp, keys kg, kg + kGroups, ... ----
+    {
+      const int cc = (2 * cp) / 8;  // 16-byte chunk of the row holding the pair
+      const int within = (2 * cp) % 8;
+      const uint8_t* vb = vs + (cc / 8) * kSwzBlockBytes + within * 2;
+#pragma unroll 4
+      for (int kk = kg; kk < kTileRows; kk += C::kGroups) {
+        const uint32_t vv = *reinterpret_cast<const uint32_t*>(vb + kk * 128 + (((cc % 8) ^ (kk & 7)) * 16));
+        const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv));
+        const float* pk = ps + kk * 8;
+        if (NQ >= 4) {
+#pragma unroll
+          for (int n4 = 0; n4 < NQ; n4 += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(pk + n4);
+            const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc[n4 + e][0] = fmaf(pp[e], vf.x, acc[n4 + e][0]);
+              acc[n4 + e][1] = fmaf(pp[e], vf.y, acc[n4 + e][1]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < NQ; ++n) {
+            acc[n][0] = fmaf(pk[n], vf.x, acc[n][0]);
+            acc[n][1] = fmaf(pk[n], vf.y, acc[n][1]);
+          }
+        }
+      }
+    }
+    __syncthreads();  // stage st and the probabilities are free again
+    if (tid == 0 && issued < t1) issue(issued);
+    ++issued;
+  }
+  if (*abort_flag) {
+    // Drain the copies still in flight (bounded) before the CTA exits: the
+    // last kStages issued, one per stage, each waited on its latest phase.
+    if (tid == 0)
+      for (int it = max(t0, min(t1, issued) - C::kStages); it < min(t1, issued); ++it) {
+        const int st = (it - t0) % C::kStages;
+        mbar_wait(&full[st], ((it - t0) / C::kStages) & 1, status);
+      }
+    return;
+  }
+
+  // ---- sum the key groups, normalise, write ----
+#pragma unroll
+  for (int n = 0; n < NQ; ++n) {
+    accs[(kg * 8 + n) * D + 2 * cp] = acc[n][0];
+    accs[(kg * 8 + n) * D + 2 * cp + 1] = acc[n][1];
+  }
+  __syncthreads();
+  for (int i = tid; i < Nq * D; i += C::kThreads) {  // i = n * D + column
+    const int n = i / D;
+    float v = 0.f;
+#pragma unroll
+    for (int g = 0; g < C::kGroups; ++g) v += accs[g * 8 * D + i];
+    float l = 0.f, m = -INFINITY;
+#pragma unroll
+    for (int nn = 0; nn < NQ; ++nn)
+      if (nn == n) {
+        l = l_run[nn];
+        m = m_run[nn];
+      }
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    const float lse2 = (l > 0.f) ? m + __log2f(l) : -INFINITY;
+    const size_t row = (size_t)bh * Nq + n;
+    if (splits == 1) {
+      o[row * D + (i - n * D)] = __float2bfloat16_rn(v * inv);
+      if (i - n * D == 0) lse[row] = lse2 * kLn2;
+    } else {
+      const size_t prow = (size_t)split * BH * Nq + row;
+      part_o[prow * D + (i - n * D)] = v * inv;
+      if (i - n * D == 0) part_lse2[prow] = lse2;
+    }
+  }
+}
+
+// One warp per (b, h, query): merge the splits' partial outputs.
+template <int D>
+__global__ void __launch_bounds__(128) fa_decode_combine(const float* __restrict__ part_o,
+                                                         const float* __restrict__ part_lse2,
+                                                         __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                         int rows, int splits) {
+  const int row = blockIdx.x * 4 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int s = lane; s < splits; s += 32) m = fmaxf(m, part_lse2[(size_t)s * rows + row]);
+#pragma unroll
+  for (int off = 16; off > 0; off /= 2) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float l = 0.f;
+  for (int s = lane; s < splits; s += 32) {
+    const float x = part_lse2[(size_t)s * rows + row];
+    l += (x == -INFINITY) ? 0.f : ex2(x - m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off /= 2) l += __shfl_xor_sync(0xffffffffu, l, off);
+  constexpr int kPer = D / 32;
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float x = part_lse2[(size_t)s * rows + row];
+    if (x == -INFINITY) continue;
+    const float w = ex2(x - m);
+    const float* src = part_o + ((size_t)s * rows + row) * D;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, src[lane + 32 * e], acc[e]);
+  }
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) o[(size_t)row * D + lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
+  if (lane == 0) lse[row] = (m + __log2f(l)) * kLn2;
+}
+
+template <int D, int NQ, bool CAUSAL>
+static cudaError_t launch_split_t(const DecLaunch& a, cudaStream_t stream) {
+  using C = DecCfg<D>;
+  auto kern = fa_decode_split<D, NQ, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<a.BH * a.splits, C::kThreads, C::kSmemBytes, stream>>>(
+      *a.tm_k, *a.tm_v, reinterpret_cast<const __nv_bfloat16*>(a.q), reinterpret_cast<__nv_bfloat16*>(a.o), a.lse,
+      a.part_o, a.part_lse2, a.BH, a.Nq, a.Nk, a.splits, a.c2, a.status);
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_split_nq(const DecLaunch& a, cudaStream_t stream) {
+  if (a.Nq <= 1) return launch_split_t<D, 1, CAUSAL>(a, stream);
+  if (a.Nq <= 2) return launch_split_t<D, 2, CAUSAL>(a, stream);
+  if (a.Nq <= 4) return launch_split_t<D, 4, CAUSAL>(a, stream);
+  return launch_split_t<D, 8, CAUSAL>(a, stream);
+}
+
+cudaError_t launch_decode(const DecLaunch& a, cudaStream_t stream) {
+  cudaError_t e;
+  if (a.d == 64)
+    e = a.causal ? launch_split_nq<64, true>(a, stream) : launch_split_nq<64, false>(a, stream);
+  else
+    e = a.causal ? launch_split_nq<128, true>(a, stream) : launch_split_nq<128, false>(a, stream);
+  if (e != cudaSuccess || a.splits == 1) return e;
+  const int rows = a.BH * a.Nq;
+  if (a.d == 64)
+    fa_decode_combine<64><<<(rows + 3) / 4, 128, 0, stream>>>(a.part_o, a.part_lse2,
+                                                              reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, rows,
+                                                              a.splits);
+  else
+    fa_decode_combine<128><<<(rows + 3) / 4, 128, 0, stream>>>(a.part_o, a.part_lse2,
+                                                               reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, rows,
+                                                               a.splits);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -46,7 +46,24 @@ struct BwdLaunch {
   int pre_grid;
 };
 
+// Split-KV forward (decode): Nq <= 8 queries per head against Nk keys.
+struct DecLaunch {
+  const CUtensorMap* tm_k;  // [BH, Nk, d] bf16, 64-column x 128-row boxes
+  const CUtensorMap* tm_v;
+  const void* q;            // [BH, Nq, d] bf16
+  void* o;                  // [BH, Nq, d] bf16
+  float* lse;               // [BH, Nq] fp32, natural log
+  float* part_o;            // [splits, BH, Nq, d] fp32 partial outputs (splits > 1)
+  float* part_lse2;         // [splits, BH, Nq] fp32 partial logsumexp, base 2 (splits > 1)
+  int BH, Nq, Nk, d;
+  int causal;
+  int splits;
+  float c2;  // scale * log2(e)
+  int* status;
+};
+
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd_conv(const BwdLaunch& a, cudaStream_t stream);

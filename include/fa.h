@@ -79,6 +79,43 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            float scale, int causal, cudaStream_t stream);
 
 /*
+ * Split-KV forward for decoding.  [L] FAQ "Does FlashAttention help during
+ * LLM decoding?": a decode step has one query (or a few) per sequence, the
+ * cost is reading the key/value cache, and Flash-Decoding spreads that read
+ * over many thread blocks.  Each split (a run of 128-key tiles of one head)
+ * computes its own softmax partial; the partials are merged with the
+ * online-softmax rescale ([T] "Softmax is the anti-tiling operation").
+ *
+ *   q         in   [B, H, Nq, d] bf16, 1 <= Nq <= 8: the last Nq positions
+ *   k, v      in   [B, H, Nk, d] bf16, the whole cache (Nk >= 1)
+ *   o         out  [B, H, Nq, d] bf16
+ *   lse       out  [B, H, Nq] fp32, natural-log logsumexp of each row
+ *   causal    key j is visible to query i iff j <= i + (Nk - Nq)
+ *             (bottom-right; needs Nq <= Nk); 0 = every key
+ *   num_splits  splits per head; 0 picks as many as fill the SMs with one
+ *             CTA each; never more than the 128-key tiles of the cache
+ *   workspace  fa_fwd_splitkv_workspace_size() bytes, 256-byte aligned,
+ *             owned by the caller (may be NULL when that size is 0)
+ *
+ * One launch when a head has one split, else two (splits, then the merge).
+ * Errors: FA_ERR_UNSUPPORTED for Nq > 8 or d not in {64, 128};
+ * FA_ERR_INVALID_ARG for non-positive sizes, causal with Nq > Nk, a negative
+ * num_splits or misaligned pointers; FA_ERR_WORKSPACE for a missing or
+ * short workspace.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                   int d, float scale, int causal, int num_splits, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
+/*
+ * Workspace bytes fa_fwd_splitkv needs for these sizes (with the current
+ * device's SM count when num_splits is 0): the fp32 partial outputs and
+ * partial logsumexps of the splits.  0 when one split per head suffices, or
+ * when the sizes are invalid (fa_fwd_splitkv then reports the error).
+ */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
  * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
  * accumulator [B, H, N, d] and the row terms D = rowsum(dO * O) [B, H, N],
  * each 256-byte aligned.  Returns 0 when the sizes are invalid.

@@ -117,3 +117,29 @@ def test_tensor_helpers_reject_cpu_tensors(lib):
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.forward(q, q, q)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=9), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(Nq=4, Nk=3, causal=1), fa.FA_ERR_INVALID_ARG),
+    (dict(num_splits=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=3), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(q=A + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+])
+def test_splitkv_validation(lib, kw, code):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=2, Nq=1, Nk=1000, d=128, scale=0.1, causal=1, num_splits=0,
+                workspace=None, workspace_bytes=0, stream=None)
+    args.update(kw)
+    assert fa.fa_fwd_splitkv(**args) == code
+
+
+def test_splitkv_workspace_size_of_invalid_sizes_is_zero(lib):
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 9, 100, 64, 0) == 0     # Nq > 8
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 1, 100, 96, 0) == 0     # d = 96
+    assert fa.fa_fwd_splitkv_workspace_size(0, 1, 1, 100, 64, 0) == 0

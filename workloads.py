@@ -106,3 +106,56 @@ def replica_seed(w: Workload, rank: int = 0) -> int:
 
 def workload_inputs(w: Workload, stress=None, rank: int = 0):
     return make_inputs(w.B, w.H, w.N, w.d, replica_seed(w, rank), stress)
+
+
+# ------------------------------------------------------------- decoding ----
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq new queries per head (the last Nq positions) against an Nk-long K/V cache."""
+    name: str
+    index: int          # seed = 2000 + index
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool = True
+    note: str = ""
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def seed(self) -> int:
+        return 2000 + self.index
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "H": self.H, "Nq": self.Nq, "Nk": self.Nk, "d": self.d,
+                "causal": self.causal, "scale": "1/sqrt(d)"}
+
+
+# Decode steps on the shapes of the measured workloads: the long-sequence head
+# shape with its whole 16384-key cache, and the GPT-2 medium batch with its
+# 1024-key cache; one query per sequence, and eight (a speculative step).
+DECODE_LONG = DecodeWorkload("decode_b1_h16_q1_k16384_d128", 0, 1, 16, 1, 16384, 128, True,
+                             "long-sequence shape at decode time: one query against a 16384-key cache")
+DECODE_GPT2 = DecodeWorkload("decode_b64_h16_q1_k1024_d64", 1, 64, 16, 1, 1024, 64, True,
+                             "GPT-2 medium batch at decode time: one query per sequence, 1024-key cache")
+DECODE_LONG_Q8 = DecodeWorkload("decode_b1_h16_q8_k16384_d128", 2, 1, 16, 8, 16384, 128, True,
+                                "long-sequence shape, eight new queries (speculative step)")
+DECODE_ALL = [DECODE_LONG, DECODE_GPT2, DECODE_LONG_Q8]
+DECODE_BY_NAME = {w.name: w for w in DECODE_ALL}
+
+
+def make_decode_inputs(B, H, Nq, Nk, d, seed, stress=None):
+    """Seeded bf16 Q [B, H, Nq, d] and K, V [B, H, Nk, d] on the CPU (drawn in that order,
+    fp32 standard normals rounded once to bf16; ``stress="wide"`` multiplies Q by 8)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q = torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    if stress == "wide":
+        q = q * 8.0
+    return tuple(t.to(torch.bfloat16) for t in (q, k, v))
