@@ -17,15 +17,18 @@
 // V, at most 8 FLOP/B: far below the tensor-core ridge, so the contractions
 // run on the CUDA cores in fp32 and the kernel is bound by HBM.
 //
-// fa_decode_split (128 threads, one CTA per (b, h, split)):
-//   scores  thread = key of the tile: s_n = c2 * q_n . k over 16-byte chunks
-//           of the swizzled K row (queries in shared memory, read as
-//           broadcasts); masked keys -inf.
+// fa_decode_split (256 threads, one CTA per (b, h, split)):
+//   scores  two threads per key of the tile, each over half of the head
+//           dimension (16-byte chunks of the swizzled K row; the queries in
+//           shared memory, halves offset by 16 banks), summed with one
+//           shuffle; masked keys -inf.
 //   softmax per query, across the CTA: tile max, rescale factor, p = 2^(s - m)
 //           into shared memory, tile sum.
 //   PV      thread = column pair x key group: acc_n += p_n(key) * v(key) over
 //           the keys of its group; groups are summed at the end.
-// fa_decode_combine: one warp per (b, h, query) merges the splits.
+// fa_decode_combine: one warp per (b, h, query) merges the splits; it is
+// launched as a programmatic dependent of the split kernel, so its launch
+// overlaps the split kernel's tail (it waits for that grid's results first).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -42,15 +45,18 @@ struct DecCfg {
   static constexpr int kTileBytes = kTileKeys * D * 2;   // one K or V tile: D / 64 swizzle blocks
   static constexpr int kBlocks = D / 64;
   static constexpr int kStages = (D == 64) ? 4 : 3;      // K+V stages in flight
-  static constexpr int kThreads = 128;
+  static constexpr int kThreads = 256;
+  static constexpr int kWarps = kThreads / 32;
+  static constexpr int kHalf = D / 2;                    // head dimensions per thread in the score phase
+  static constexpr int kQHalfStride = 8 * kHalf + 16;    // floats between the two halves of the queries
   static constexpr int kPairs = D / 2;                   // column pairs (PV phase)
-  static constexpr int kGroups = kThreads / kPairs;      // key groups (PV phase): 2 at d = 128, 4 at d = 64
+  static constexpr int kGroups = kThreads / kPairs;      // key groups (PV phase): 4 at d = 128, 8 at d = 64
   static constexpr int kOffK = 0;                                  // [stages] K tiles
   static constexpr int kOffV = kOffK + kStages * kTileBytes;       // [stages] V tiles
-  static constexpr int kOffQ = kOffV + kStages * kTileBytes;       // [8][D] fp32 queries
-  static constexpr int kOffP = kOffQ + 8 * D * 4;                  // [128 keys][8] fp32 probabilities
-  static constexpr int kOffRed = kOffP + kTileKeys * 8 * 4;        // [2][4 warps][8] fp32 reductions
-  static constexpr int kOffAcc = kOffRed + 2 * 4 * 8 * 4;          // [groups][8][D] fp32 partial outputs
+  static constexpr int kOffQ = kOffV + kStages * kTileBytes;       // [2 halves][8][D / 2] fp32 queries (+pad)
+  static constexpr int kOffP = kOffQ + 2 * kQHalfStride * 4;       // [128 keys][8] fp32 probabilities
+  static constexpr int kOffRed = kOffP + kTileKeys * 8 * 4;        // [2][warps][8] fp32 reductions
+  static constexpr int kOffAcc = kOffRed + 2 * kWarps * 8 * 4;     // [groups][8][D] fp32 partial outputs
   static constexpr int kOffBar = kOffAcc + kGroups * 8 * D * 4;    // [stages] mbarriers
   static constexpr int kOffAbort = kOffBar + 8 * kStages;
   static constexpr int kSmemBytes = kOffAbort + 16;
@@ -60,7 +66,7 @@ struct DecCfg {
 
 // NQ: queries handled (Nq rounded up to 1, 2, 4 or 8; slots past Nq stay masked).
 template <int D, int NQ, bool CAUSAL>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     fa_decode_split(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                     float* __restrict__ part_o, float* __restrict__ part_lse2, int BH, int Nq, int Nk, int splits,
@@ -91,10 +97,13 @@ __global__ void __launch_bounds__(128, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // Queries -> fp32 in shared memory (slots past Nq are zero and stay masked).
+  // Queries -> fp32 in shared memory as [half][query][D / 2] (slots past Nq
+  // are zero and stay masked).
   for (int i = tid; i < NQ * D; i += C::kThreads) {
-    const int n = i / D;
-    qs[i] = (n < Nq) ? __bfloat162float(q[((size_t)bh * Nq + n) * D + (i - n * D)]) : 0.f;
+    const int n = i / D, col = i - n * D;
+    const int h = col / C::kHalf;
+    qs[h * C::kQHalfStride + n * C::kHalf + (col - h * C::kHalf)] =
+        (n < Nq) ? __bfloat162float(q[((size_t)bh * Nq + n) * D + col]) : 0.f;
   }
   __syncthreads();
   auto issue = [&](int it) {  // tile it into its stage
@@ -124,7 +133,6 @@ __global__ void __launch_bounds__(128, 1)
   float acc[NQ][2];
 #pragma unroll
   for (int n = 0; n < NQ; ++n) acc[n][0] = acc[n][1] = 0.f;
-  const int swz = tid & 7;
 
   int issued = min(t1, t0 + C::kStages);
   for (int it = t0; it < t1; ++it) {
@@ -135,15 +143,22 @@ __global__ void __launch_bounds__(128, 1)
     const uint8_t* ks = sm + C::kOffK + st * C::kTileBytes;
     const uint8_t* vs = sm + C::kOffV + st * C::kTileBytes;
 
-    // ---- scores: thread = key ----
-    const int key = it * kTileRows + tid;
-    float sc[NQ];
+    // ---- scores: two threads per key, each over half of the head dimension ----
+    // d = 128: half h is swizzle block h, its chunks taken in the order i ^ 4h;
+    // d = 64: half h is chunks 4h .. 4h + 3 of the one block.  Either way the
+    // eight threads of a quarter-warp hit eight different chunk positions.
+    const int kr = tid >> 1, half = tid & 1;
+    const int key = it * kTileRows + kr;
+    const float* qh = qs + half * C::kQHalfStride;
+    float sa[NQ], sb[NQ];  // two partial sums per query (shorter dependency chains)
 #pragma unroll
-    for (int n = 0; n < NQ; ++n) sc[n] = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 kv = *reinterpret_cast<const uint4*>(ks + (c / 8) * kSwzBlockBytes + tid * 128 +
-                                                       (((c % 8) ^ swz) * 16));
+    for (int n = 0; n < NQ; ++n) sa[n] = sb[n] = 0.f;
+#pragma unroll
+    for (int i = 0; i < C::kHalf / 8; ++i) {
+      const int ck = (D == 128) ? (i ^ (4 * half)) : (4 * half + i);  // chunk of the 128-byte row
+      const int qc = (D == 128) ? (i ^ (4 * half)) : i;               // chunk within the half
+      const uint4 kv = *reinterpret_cast<const uint4*>(ks + ((D == 128) ? half * kSwzBlockBytes : 0) + kr * 128 +
+                                                       ((ck ^ (kr & 7)) * 16));
       const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&kv);
       float kf[8];
 #pragma unroll
@@ -154,22 +169,26 @@ __global__ void __launch_bounds__(128, 1)
       }
 #pragma unroll
       for (int n = 0; n < NQ; ++n) {
-        const float4 qa = *reinterpret_cast<const float4*>(qs + n * D + 8 * c);
-        const float4 qb = *reinterpret_cast<const float4*>(qs + n * D + 8 * c + 4);
-        sc[n] = fmaf(qa.x, kf[0], sc[n]);
-        sc[n] = fmaf(qa.y, kf[1], sc[n]);
-        sc[n] = fmaf(qa.z, kf[2], sc[n]);
-        sc[n] = fmaf(qa.w, kf[3], sc[n]);
-        sc[n] = fmaf(qb.x, kf[4], sc[n]);
-        sc[n] = fmaf(qb.y, kf[5], sc[n]);
-        sc[n] = fmaf(qb.z, kf[6], sc[n]);
-        sc[n] = fmaf(qb.w, kf[7], sc[n]);
+        const float4 qa = *reinterpret_cast<const float4*>(qh + n * C::kHalf + 8 * qc);
+        const float4 qb = *reinterpret_cast<const float4*>(qh + n * C::kHalf + 8 * qc + 4);
+        float& acc_s = (i & 1) ? sb[n] : sa[n];
+        acc_s = fmaf(qa.x, kf[0], acc_s);
+        acc_s = fmaf(qa.y, kf[1], acc_s);
+        acc_s = fmaf(qa.z, kf[2], acc_s);
+        acc_s = fmaf(qa.w, kf[3], acc_s);
+        acc_s = fmaf(qb.x, kf[4], acc_s);
+        acc_s = fmaf(qb.y, kf[5], acc_s);
+        acc_s = fmaf(qb.z, kf[6], acc_s);
+        acc_s = fmaf(qb.w, kf[7], acc_s);
       }
     }
+    float sc[NQ];
 #pragma unroll
     for (int n = 0; n < NQ; ++n) {
+      const float part = sa[n] + sb[n];
+      const float full_dot = part + __shfl_xor_sync(0xffffffffu, part, 1);
       const bool vis = n < Nq && key < kend && (!CAUSAL || key <= n + shift);
-      sc[n] = vis ? sc[n] * c2 : -INFINITY;
+      sc[n] = vis ? full_dot * c2 : -INFINITY;
     }
     // ---- tile maximum per query, across the CTA ----
 #pragma unroll
@@ -183,20 +202,25 @@ __global__ void __launch_bounds__(128, 1)
     float m_new[NQ], alpha[NQ];
 #pragma unroll
     for (int n = 0; n < NQ; ++n) {
-      const float mt = fmaxf(fmaxf(red[n], red[8 + n]), fmaxf(red[16 + n], red[24 + n]));
+      float mt = red[n];
+#pragma unroll
+      for (int w = 1; w < C::kWarps; ++w) mt = fmaxf(mt, red[w * 8 + n]);
       m_new[n] = fmaxf(m_run[n], mt);
       alpha[n] = (m_run[n] == m_new[n]) ? 1.f : ex2(m_run[n] - m_new[n]);  // 0 when m_run = -inf
-      const float p = (sc[n] == -INFINITY) ? 0.f : ex2(sc[n] - m_new[n]);
-      ps[tid * 8 + n] = p;
+      // both threads of a key hold its score; the first one stores and counts it
+      const float p = (sc[n] == -INFINITY || half) ? 0.f : ex2(sc[n] - m_new[n]);
+      if (!half) ps[kr * 8 + n] = p;
       float sum = p;
 #pragma unroll
       for (int off = 16; off > 0; off /= 2) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (lane == 0) red[32 + warp * 8 + n] = sum;
+      if (lane == 0) red[C::kWarps * 8 + warp * 8 + n] = sum;
     }
     __syncthreads();
 #pragma unroll
     for (int n = 0; n < NQ; ++n) {
-      const float lt = (red[32 + n] + red[40 + n]) + (red[48 + n] + red[56 + n]);
+      float lt = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::kWarps; ++w) lt += red[C::kWarps * 8 + w * 8 + n];
       l_run[n] = alpha[n] * l_run[n] + lt;
       m_run[n] = m_new[n];
       acc[n][0] *= alpha[n];
@@ -247,6 +271,9 @@ __global__ void __launch_bounds__(128, 1)
     return;
   }
 
+  // The merge kernel (a programmatic dependent) may start launching now; it
+  // waits for this grid's results before reading them.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- sum the key groups, normalise, write ----
 #pragma unroll
   for (int n = 0; n < NQ; ++n) {
@@ -286,6 +313,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine(const float* __restrict
                                                          const float* __restrict__ part_lse2,
                                                          __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                                          int rows, int splits) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the split kernel's partials are complete
   const int row = blockIdx.x * 4 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (row >= rows) return;
@@ -346,15 +374,21 @@ cudaError_t launch_decode(const DecLaunch& a, cudaStream_t stream) {
     e = a.causal ? launch_split_nq<128, true>(a, stream) : launch_split_nq<128, false>(a, stream);
   if (e != cudaSuccess || a.splits == 1) return e;
   const int rows = a.BH * a.Nq;
-  if (a.d == 64)
-    fa_decode_combine<64><<<(rows + 3) / 4, 128, 0, stream>>>(a.part_o, a.part_lse2,
-                                                              reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, rows,
-                                                              a.splits);
-  else
-    fa_decode_combine<128><<<(rows + 3) / 4, 128, 0, stream>>>(a.part_o, a.part_lse2,
-                                                               reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, rows,
-                                                               a.splits);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* po = a.part_o;
+  const float* pl = a.part_lse2;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o);
+  if (a.d == 64) return cudaLaunchKernelEx(&cfg, fa_decode_combine<64>, po, pl, out, a.lse, rows, a.splits);
+  return cudaLaunchKernelEx(&cfg, fa_decode_combine<128>, po, pl, out, a.lse, rows, a.splits);
 }
 
 }  // namespace fa
