@@ -479,9 +479,6 @@ def run_decode(args, w):
     nbytes = decode_bytes(w)
     value = nbytes / (ms * 1e-3) / 1e9
     peaks, peak_src = load_peaks()
-    # splits per head under the automatic choice (the library's rule: one CTA per SM, at most one per tile)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    nsplit = min((w.Nk + 127) // 128, max(1, sms // (w.B * w.H)))
     # ---- end to end: the cache and queries from pinned host memory, results back ----
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
@@ -510,7 +507,10 @@ def run_decode(args, w):
     line = {"metric": DECODE_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
-            "config": {**w.describe(), "parallelism": "single GPU", "splits_per_head": int(nsplit),
+            "config": {**w.describe(), "parallelism": "single GPU",
+                       "splits": "chosen by the library (num_splits = 0)",
+                       "merge": ("no workspace (one split per head, or a head's splits merge in one cluster)"
+                                 if ws_bytes == 0 else "workspace + merge kernel"),
                        "l2": "flushed before every timed step (2x L2 buffer written)",
                        "bytes_per_step": nbytes},
             "roofline": {"kernel": "fa_decode_split (+ fa_decode_combine)", "bound": "hbm",

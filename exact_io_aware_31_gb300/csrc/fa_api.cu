@@ -200,18 +200,60 @@ int check_decode(int B, int H, int Nq, int Nk, int d, float scale, int causal, i
   return FA_OK;
 }
 
-// Splits actually used: the requested number, or (0) as many as fill the SMs
-// with one CTA each; never more than the 128-key tiles of the cache.
-int decode_splits(long long bh, int Nk, int num_splits, int sms) {
-  const int tiles = (Nk + 127) / 128;
-  long long s = num_splits > 0 ? num_splits : (sms / bh > 1 ? sms / bh : 1);
-  if (s > tiles) s = tiles;
-  return (int)s;
+// Clusters of `size` decode split CTAs the device can hold at once, for both
+// masks (the smaller count); asked once per (device, d, query bucket, size).
+int decode_cluster_capacity(int dev, int d, int Nq, int size) {
+  if (size < 2 || size > 16) return 0;
+  static std::mutex mu;
+  static int known[kMaxDevices][2][4][17];  // capacity + 1; 0 = not asked yet
+  const int qb = Nq <= 1 ? 0 : Nq <= 2 ? 1 : Nq <= 4 ? 2 : 3;
+  std::lock_guard<std::mutex> lock(mu);
+  int& k = known[dev][d == 128][qb][size];
+  if (k == 0) {
+    const int a = decode_max_clusters(d, Nq, 0, size), b = decode_max_clusters(d, Nq, 1, size);
+    k = (a < b ? a : b) + 1;
+  }
+  return k - 1;
 }
 
-size_t decode_partials_bytes(long long bh, int Nq, int d, int splits) {
-  if (splits <= 1) return 0;
+// Splits per head and whether they merge inside one cluster.  The requested
+// number (never more than the 128-key tiles), or (0) as many as fill the SMs
+// with one CTA each.  A head's splits run as one cluster when every head's
+// cluster fits on the device at once; the automatic choice takes down to 80%
+// of its split count to get there (the cluster merge saves the second kernel
+// and its launch gap).  Otherwise the splits merge through the workspace.
+int decode_plan(int dev, long long bh, int Nq, int Nk, int d, int num_splits, int sms, bool* cluster) {
+  const int tiles = (Nk + 127) / 128;
+  *cluster = false;
+  if (num_splits > 0) {
+    const int s = num_splits < tiles ? num_splits : tiles;
+    *cluster = s >= 2 && decode_cluster_capacity(dev, d, Nq, s) >= bh;
+    return s;
+  }
+  long long s0 = sms / bh > 1 ? sms / bh : 1;
+  if (s0 > tiles) s0 = tiles;
+  if (s0 < 2) return (int)s0;
+  const int lo = (int)((4 * s0 + 4) / 5) > 2 ? (int)((4 * s0 + 4) / 5) : 2;
+  for (int s = (int)(s0 < 16 ? s0 : 16); s >= lo; --s)
+    if (decode_cluster_capacity(dev, d, Nq, s) >= bh) {
+      *cluster = true;
+      return s;
+    }
+  return (int)s0;
+}
+
+size_t decode_partials_bytes(long long bh, int Nq, int d, int splits, bool cluster) {
+  if (splits <= 1 || cluster) return 0;
   return round256((size_t)splits * bh * Nq * d * 4) + round256((size_t)splits * bh * Nq * 4);
+}
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return dev;
 }
 
 }  // namespace
@@ -222,7 +264,9 @@ extern "C" size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, in
   DeviceInfo* dev = nullptr;
   if (device_info(&dev) != FA_OK) return 0;
   const long long bh = (long long)B * H;
-  return decode_partials_bytes(bh, Nq, d, decode_splits(bh, Nk, num_splits, dev->sms));
+  bool cluster = false;
+  const int splits = decode_plan(current_device(), bh, Nq, Nk, d, num_splits, dev->sms, &cluster);
+  return decode_partials_bytes(bh, Nq, d, splits, cluster);
 }
 
 extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
@@ -235,8 +279,10 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   if ((st = device_info(&dev)) != FA_OK) return st;
   const int BH = B * H;
   DecLaunch a;
-  a.splits = decode_splits(BH, Nk, num_splits, dev->sms);
-  const size_t need = decode_partials_bytes(BH, Nq, d, a.splits);
+  bool cluster = false;
+  a.splits = decode_plan(current_device(), BH, Nq, Nk, d, num_splits, dev->sms, &cluster);
+  a.cluster = cluster ? 1 : 0;
+  const size_t need = decode_partials_bytes(BH, Nq, d, a.splits, cluster);
   if (need > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                    workspace_bytes < need))
     return FA_ERR_WORKSPACE;

@@ -74,6 +74,9 @@ constexpr int kBwdPolyEvery = FA_BWD_POLY_EVERY;
 // d = 128; warpgroup g owns query columns [g 128/n, (g+1) 128/n) of every
 // tile.  More warpgroups hide more of the TMEM-load, MUFU and shared-memory
 // latency of the P and dS phases, at fewer registers per thread.
+#ifndef FA_BWD_DS_TMEM
+#define FA_BWD_DS_TMEM 0
+#endif
 #ifndef FA_BWD_COMPUTE_WG_D64
 #define FA_BWD_COMPUTE_WG_D64 2
 #endif
@@ -185,6 +188,12 @@ struct BwdCfg {
   static constexpr int kColDV = 256;
   static constexpr int kColDK = 256 + D;
   static constexpr int kColDQ = kDqAliasesDp ? kColDP : 256 + 2 * D;
+  // d = 64 with FA_BWD_DS_TMEM: dS^T also packed as bf16 pairs in the last 64
+  // columns, so dK takes its A operand from TMEM instead of shared memory
+  // (d = 128 has no room).  Measured slower (the extra TMEM store sits on the
+  // compute warps' path), so off.
+  static constexpr bool kDsTmem = (D == 64) && (FA_BWD_DS_TMEM != 0);
+  static constexpr int kColDST = 256 + 3 * D;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKvStages * kTileBytes;
   static constexpr int kOffQ = kOffV + kKvStages * kTileBytes;    // [stages]
@@ -204,12 +213,13 @@ struct BwdCfg {
   static constexpr int kOffRow = kOffDQS + kDqStageBytes;        // [stages][lse2 128 | D 128] fp32
   static constexpr int kRowBytes = 2 * kTileRows * 4;
   static constexpr int kOffBar = kOffRow + kStages * kRowBytes;
-  static constexpr int kNumBars = 2 * kKvStages + 3 * kStages + 15;
+  static constexpr int kNumBars = 2 * kKvStages + 3 * kStages + 16;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kColDQ + D <= kTmemCols, "tensor memory budget");
+  static_assert(!kDsTmem || (kColDST >= kColDQ + D && kColDST + 64 <= kTmemCols), "dS^T columns");
 };
 
 struct BwdUnit {
@@ -280,6 +290,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   uint64_t* dqs_full = s_full + 12;  // d = 64: a dQ partial staged (128 arrivals)
   uint64_t* dqs_free = s_full + 13;  // d = 64: the staging buffer is free
   uint64_t* ds_empty2 = s_full + 14;  // second dS buffer (d = 64)
+  uint64_t* dst_empty = s_full + 15;  // dS^T in TMEM read by dK (d = 64)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
 
@@ -305,6 +316,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(ds_full, C::kComputeThreads);
     mbar_init(ds_empty, 1);
     mbar_init(ds_empty2, 1);
+    mbar_init(dst_empty, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, C::kDqWarpgroup ? 128 : C::kComputeThreads);
     mbar_init(dkdv_full, 1);
@@ -530,10 +542,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t dsb = ds_s + db * C::kDsBytes;
+          if (C::kDsTmem) {
+            // dK += dS^T Q with dS^T from TMEM (8 packed columns per 16 queries)
 #pragma unroll
-          for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ss(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
-                   sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+            for (int k = 0; k < kTileRows / 16; ++k)
+              mma_ts(tbase + C::kColDK, tbase + C::kColDST + 8 * k,
+                     sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+            mma_commit(dst_empty);  // dS^T in TMEM may be overwritten once dK(i) is done
+          } else {
+#pragma unroll
+            for (int k = 0; k < kTileRows / 16; ++k)
+              mma_ss(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
+                     sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+          }
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k) {
             const uint64_t dsd = sdesc(dsb + k * 2048, kSwzBlockBytes, 1024);  // dS^T, 16 keys
@@ -575,6 +596,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + kQC * g);
     const uint32_t t_dv = tmem_lane_col(tbase, lanes, C::kColDV + kDC * g);
     const uint32_t t_dk = tmem_lane_col(tbase, lanes, C::kColDK + kDC * g);
+    const uint32_t t_dst = tmem_lane_col(tbase, lanes, C::kColDST + (kQC / 2) * g);  // packed dS^T (d = 64)
     // dS^T row r in shared memory: query q is 16-byte chunk q / 8 of the row,
     // in swizzle block (q / 8) / 8 at position (q / 8) % 8.
     const int chunk0 = kQC * g / 8;
@@ -583,6 +605,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int swz = r & 7;
     const uint64_t c2x2 = f2_pack(c2, c2);
     uint32_t scnt = 0, dpcnt = 0, dse = 0, ucnt = 0, qit = 0, dqcnt = 0;
+    uint32_t dstc = 0;        // d = 64: dS^T tiles written to TMEM
     uint32_t ecnt = 0;        // d = 64: units whose dK / dV went out through the dS buffer
     bool epi_pending = false;  // ... the last of which may still be reading it
     int pend_bh = 0, pend_qt = -1;  // dQ partial still to drain from the previous unit
@@ -640,14 +663,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         uint32_t pk[kQC / 2];  // this warpgroup's P^T row, bf16 pairs (reused for dS)
+        uint32_t svall[kQC];   // the whole S^T row piece: every load in flight, one wait
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c) tmem_ld32(t_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&svall[32 * c]));
+        tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < kQC / 32; ++c) {
-          uint32_t sv[32];
-          tmem_ld32(t_s + 32 * c, sv);
-          tmem_wait_ld();
+          const uint32_t* sv = svall + 32 * c;
+          // -lse2 of the 32 queries, four per 16-byte broadcast load
+          ulonglong2 nlv[8];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) nlv[e4] = *reinterpret_cast<const ulonglong2*>(rows + 32 * c + 4 * e4);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(rows + 32 * c + 2 * e);
+            const uint64_t nl2 = (e & 1) ? nlv[e / 2].y : nlv[e / 2].x;
             const uint64_t xx = f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2x2, nl2);
             float p0, p1;
             if (kBwdPolyEvery > 0 && full_tile && (e % kBwdPolyMod) == kBwdPolyMod - 1) {
@@ -704,28 +733,44 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tr(4);
         if (!ok) break;
         tc_fence_after();
+        uint32_t dpall[kQC];  // the whole dP^T row piece: every load in flight, one wait
+#pragma unroll
+        for (int c = 0; c < kQC / 32; ++c) tmem_ld32(t_dp + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&dpall[32 * c]));
+        tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < kQC / 32; ++c) {
-          uint32_t dpv[32];
-          tmem_ld32(t_dp + 32 * c, dpv);
-          tmem_wait_ld();
+          const uint32_t* dpv = dpall + 32 * c;
 #pragma unroll
           for (int mm = 0; mm < 4; ++mm) {  // four 16-byte chunks = 32 queries
             const int m = 4 * c + mm;
             uint32_t dsk[4];
+            // -D of the chunk's 8 queries, four per 16-byte broadcast load
+            const ulonglong2 nd01 = *reinterpret_cast<const ulonglong2*>(rows + kTileRows + 8 * m);
+            const ulonglong2 nd23 = *reinterpret_cast<const ulonglong2*>(rows + kTileRows + 8 * m + 4);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int idx = 4 * m + e;  // pair index within the half
-              const uint64_t nd = *reinterpret_cast<const uint64_t*>(rows + kTileRows + 2 * idx);
+              const uint64_t nd = (e == 0) ? nd01.x : (e == 1) ? nd01.y : (e == 2) ? nd23.x : nd23.y;
               const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[idx]));
               const uint64_t t =
                   f2_add(f2_pack(__uint_as_float(dpv[8 * mm + 2 * e]), __uint_as_float(dpv[8 * mm + 2 * e + 1])), nd);
               float d0, d1;
               f2_unpack(f2_mul(f2_pack(pf.x, pf.y), t), d0, d1);
               dsk[e] = pack_bf16x2(d0, d1);
+              if (C::kDsTmem) pk[idx] = dsk[e];  // P^T is no longer needed: keep dS^T for TMEM
             }
             *reinterpret_cast<uint4*>(ds_row + (((cbase + m) ^ swz) * 16)) = make_uint4(dsk[0], dsk[1], dsk[2], dsk[3]);
           }
+        }
+        if (C::kDsTmem) {
+          // dS^T also into TMEM (the A operand of dK), once dK of the previous
+          // tile has read it there.
+          if (!(ok = mbar_wait_warp(dst_empty, (dstc & 1) ^ 1, status))) break;
+          ++dstc;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < kQC / 32; ++c) tmem_st16(t_dst + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
+          tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before();

@@ -26,9 +26,13 @@
 //           into shared memory, tile sum.
 //   PV      thread = column pair x key group: acc_n += p_n(key) * v(key) over
 //           the keys of its group; groups are summed at the end.
-// fa_decode_combine: one warp per (b, h, query) merges the splits; it is
-// launched as a programmatic dependent of the split kernel, so its launch
-// overlaps the split kernel's tail (it waits for that grid's results first).
+// Merging: when a head's splits fit in one thread-block cluster (at most 16
+// CTAs that the device can co-schedule), they are launched as one and rank 0
+// merges the partials from the other CTAs' shared memory; no workspace, no
+// second kernel.  Otherwise each split writes its partial to the workspace and
+// fa_decode_combine (one warp per (b, h, query)) merges them; it is launched
+// as a programmatic dependent of the split kernel, so its launch overlaps the
+// split kernel's tail (it waits for that grid's results first).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,7 +48,11 @@ struct DecCfg {
   static constexpr int kTileKeys = kTileRows;            // 128 keys per tile
   static constexpr int kTileBytes = kTileKeys * D * 2;   // one K or V tile: D / 64 swizzle blocks
   static constexpr int kBlocks = D / 64;
-  static constexpr int kStages = (D == 64) ? 4 : 3;      // K+V stages in flight
+  // K+V stages in flight: 3 x 64 KB at d = 128 (one CTA per SM); 2 x 32 KB at
+  // d = 64, small enough for two CTAs per SM (one filling its pipeline while
+  // the other streams).
+  static constexpr int kStages = (D == 64) ? 2 : 3;
+  static constexpr int kCtasPerSm = (D == 64) ? 2 : 1;
   static constexpr int kThreads = 256;
   static constexpr int kWarps = kThreads / 32;
   static constexpr int kHalf = D / 2;                    // head dimensions per thread in the score phase
@@ -57,20 +65,21 @@ struct DecCfg {
   static constexpr int kOffP = kOffQ + 2 * kQHalfStride * 4;       // [128 keys][8] fp32 probabilities
   static constexpr int kOffRed = kOffP + kTileKeys * 8 * 4;        // [2][warps][8] fp32 reductions
   static constexpr int kOffAcc = kOffRed + 2 * kWarps * 8 * 4;     // [groups][8][D] fp32 partial outputs
-  static constexpr int kOffBar = kOffAcc + kGroups * 8 * D * 4;    // [stages] mbarriers
+  static constexpr int kOffMrg = kOffAcc + kGroups * 8 * D * 4;    // [8][D] partial output + [8] lse2 (cluster merge)
+  static constexpr int kOffBar = kOffMrg + (8 * D + 8) * 4;        // [stages] mbarriers
   static constexpr int kOffAbort = kOffBar + 8 * kStages;
   static constexpr int kSmemBytes = kOffAbort + 16;
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kSmemBytes * kCtasPerSm <= 232448, "shared memory budget");
   static_assert(kGroups * kPairs == kThreads, "PV mapping");
 };
 
 // NQ: queries handled (Nq rounded up to 1, 2, 4 or 8; slots past Nq stay masked).
 template <int D, int NQ, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, (D == 64 && NQ <= 4) ? 2 : 1)
     fa_decode_split(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                     float* __restrict__ part_o, float* __restrict__ part_lse2, int BH, int Nq, int Nk, int splits,
-                    float c2, int* status) {
+                    int cluster_merge, float c2, int* status) {
   using C = DecCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
@@ -79,6 +88,7 @@ __global__ void __launch_bounds__(256, 1)
   float* ps = reinterpret_cast<float*>(sm + C::kOffP);
   float* red = reinterpret_cast<float*>(sm + C::kOffRed);
   float* accs = reinterpret_cast<float*>(sm + C::kOffAcc);
+  float* mrg = reinterpret_cast<float*>(sm + C::kOffMrg);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
 
@@ -268,6 +278,10 @@ __global__ void __launch_bounds__(256, 1)
         const int st = (it - t0) % C::kStages;
         mbar_wait(&full[st], ((it - t0) / C::kStages) & 1, status);
       }
+    if (cluster_merge) {  // the other CTAs of the cluster wait for this one at both barriers
+      cluster_sync_all();
+      cluster_sync_all();
+    }
     return;
   }
 
@@ -299,11 +313,40 @@ __global__ void __launch_bounds__(256, 1)
     if (splits == 1) {
       o[row * D + (i - n * D)] = __float2bfloat16_rn(v * inv);
       if (i - n * D == 0) lse[row] = lse2 * kLn2;
+    } else if (cluster_merge) {
+      mrg[i] = v * inv;
+      if (i - n * D == 0) mrg[8 * D + n] = lse2;
     } else {
       const size_t prow = (size_t)split * BH * Nq + row;
       part_o[prow * D + (i - n * D)] = v * inv;
       if (i - n * D == 0) part_lse2[prow] = lse2;
     }
+  }
+  if (cluster_merge) {
+    // The splits of this head form one cluster (rank = split): rank 0 merges
+    // the partials straight from the other CTAs' shared memory, with the
+    // online-softmax rescale (weights 2^(lse2_r - max)).
+    cluster_sync_all();  // every partial is written and visible cluster-wide
+    if (cluster_rank() == 0) {
+      const uint32_t mrg_addr = smem_addr(mrg);
+      for (int i = tid; i < Nq * D; i += C::kThreads) {
+        const int n = i / D;
+        float m = -INFINITY;
+        for (int r = 0; r < splits; ++r) m = fmaxf(m, ld_cluster_f32(mrg_addr + (8 * D + n) * 4, r));
+        float l = 0.f, v = 0.f;
+        for (int r = 0; r < splits; ++r) {
+          const float x = ld_cluster_f32(mrg_addr + (8 * D + n) * 4, r);
+          if (x == -INFINITY) continue;
+          const float w = ex2(x - m);
+          l += w;
+          v = fmaf(w, ld_cluster_f32(mrg_addr + i * 4, r), v);
+        }
+        const size_t row = (size_t)bh * Nq + n;
+        o[row * D + (i - n * D)] = __float2bfloat16_rn(v / l);
+        if (i - n * D == 0) lse[row] = (m + __log2f(l)) * kLn2;
+      }
+    }
+    cluster_sync_all();  // keep every CTA's shared memory alive until rank 0 has read it
   }
 }
 
@@ -347,15 +390,77 @@ __global__ void __launch_bounds__(128) fa_decode_combine(const float* __restrict
 }
 
 template <int D, int NQ, bool CAUSAL>
-static cudaError_t launch_split_t(const DecLaunch& a, cudaStream_t stream) {
+static cudaError_t prepare_split_t(int cluster) {
   using C = DecCfg<D>;
   auto kern = fa_decode_split<D, NQ, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e == cudaSuccess && cluster > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+template <int D, int NQ, bool CAUSAL>
+static cudaError_t launch_split_t(const DecLaunch& a, cudaStream_t stream) {
+  using C = DecCfg<D>;
+  auto kern = fa_decode_split<D, NQ, CAUSAL>;
+  cudaError_t e = prepare_split_t<D, NQ, CAUSAL>(a.cluster ? a.splits : 1);
   if (e != cudaSuccess) return e;
-  kern<<<a.BH * a.splits, C::kThreads, C::kSmemBytes, stream>>>(
-      *a.tm_k, *a.tm_v, reinterpret_cast<const __nv_bfloat16*>(a.q), reinterpret_cast<__nv_bfloat16*>(a.o), a.lse,
-      a.part_o, a.part_lse2, a.BH, a.Nq, a.Nk, a.splits, a.c2, a.status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.BH * a.splits);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of one head form a cluster
+  attr[0].val.clusterDim.x = a.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.cluster ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, *a.tm_k, *a.tm_v, reinterpret_cast<const __nv_bfloat16*>(a.q),
+                            reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, a.part_o, a.part_lse2, a.BH, a.Nq, a.Nk,
+                            a.splits, a.cluster, a.c2, a.status);
+}
+
+// Clusters of `cluster` split CTAs of this kernel that can be resident at
+// once (0: not launchable as a cluster).
+template <int D, int NQ, bool CAUSAL>
+static int max_clusters_t(int cluster) {
+  using C = DecCfg<D>;
+  if (prepare_split_t<D, NQ, CAUSAL>(cluster) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fa_decode_split<D, NQ, CAUSAL>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int D, bool CAUSAL>
+static int max_clusters_nq(int nq, int cluster) {
+  if (nq <= 1) return max_clusters_t<D, 1, CAUSAL>(cluster);
+  if (nq <= 2) return max_clusters_t<D, 2, CAUSAL>(cluster);
+  if (nq <= 4) return max_clusters_t<D, 4, CAUSAL>(cluster);
+  return max_clusters_t<D, 8, CAUSAL>(cluster);
+}
+
+int decode_max_clusters(int d, int nq, int causal, int cluster) {
+  if (cluster < 2 || cluster > 16) return 0;
+  if (d == 64) return causal ? max_clusters_nq<64, true>(nq, cluster) : max_clusters_nq<64, false>(nq, cluster);
+  return causal ? max_clusters_nq<128, true>(nq, cluster) : max_clusters_nq<128, false>(nq, cluster);
 }
 
 template <int D, bool CAUSAL>
@@ -372,7 +477,7 @@ cudaError_t launch_decode(const DecLaunch& a, cudaStream_t stream) {
     e = a.causal ? launch_split_nq<64, true>(a, stream) : launch_split_nq<64, false>(a, stream);
   else
     e = a.causal ? launch_split_nq<128, true>(a, stream) : launch_split_nq<128, false>(a, stream);
-  if (e != cudaSuccess || a.splits == 1) return e;
+  if (e != cudaSuccess || a.splits == 1 || a.cluster) return e;
   const int rows = a.BH * a.Nq;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((rows + 3) / 4);

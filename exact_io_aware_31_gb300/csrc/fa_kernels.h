@@ -58,12 +58,15 @@ struct DecLaunch {
   int BH, Nq, Nk, d;
   int causal;
   int splits;
+  int cluster;  // 1: the splits of a head run as one cluster and merge in shared memory
   float c2;  // scale * log2(e)
   int* status;
 };
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecLaunch& a, cudaStream_t stream);
+// Clusters of `cluster` decode split CTAs that can be resident at once (0: none).
+int decode_max_clusters(int d, int nq, int causal, int cluster);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd_conv(const BwdLaunch& a, cudaStream_t stream);

@@ -90,16 +90,30 @@ __device__ __forceinline__ bool mbar_probe(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// Tuning knob: the spin of the bounded waits below tests with try_wait (0,
+// may suspend the thread until the phase completes) or with the
+// non-blocking test_wait (1, pure polling).
+#ifndef FA_WAIT_POLL
+#define FA_WAIT_POLL 0
+#endif
+__device__ __forceinline__ bool mbar_spin_test(uint32_t addr, uint32_t parity) {
+#if FA_WAIT_POLL
+  return mbar_probe(addr, parity);
+#else
+  return mbar_test(addr, parity);
+#endif
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (after recording kDevTimeout in *status) if it has not within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
   const uint32_t a = smem_addr(bar);
-  if (mbar_test(a, parity)) return true;
+  if (mbar_spin_test(a, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_test(a, parity)) return true;
+      if (mbar_spin_test(a, parity)) return true;
     if (global_ns() - t0 > kWaitLimitNs) {
       atomicExch(status, kDevTimeout);
       return false;
@@ -113,13 +127,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 // broadcast, so a timeout is also warp-uniform.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status) {
   const uint32_t a = smem_addr(bar);
-  bool done = mbar_test(a, parity);
+  bool done = mbar_spin_test(a, parity);
   if (__all_sync(0xffffffffu, done)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i) {
-      done = done || mbar_test(a, parity);
+      done = done || mbar_spin_test(a, parity);
       if (__all_sync(0xffffffffu, done)) return true;
     }
     const bool expired = __shfl_sync(0xffffffffu, (global_ns() - t0 > kWaitLimitNs) ? 1 : 0, 0) != 0;
@@ -197,6 +211,25 @@ __device__ __forceinline__ void tma_store_wait_read0() {
 
 // Wait until all committed stores are complete (visible in global memory).
 __device__ __forceinline__ void tma_store_wait_all0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ------------------------------------------------------- thread-block clusters ---
+// Every thread of every CTA of the cluster arrives (release) and waits (acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// fp32 at this CTA's shared address `addr`, as seen in cluster CTA `rank`.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr, int rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
 
 // ---------------------------------------------------------------- tcgen05 ---
 // TMEM address: bits 31..16 lane, bits 15..0 column (32-bit columns).

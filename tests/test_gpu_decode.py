@@ -3,8 +3,10 @@
 Cases span: one and several queries (Nq = 1..8, rounded up inside to 1, 2, 4
 or 8), ragged caches (Nk not a multiple of 128, Nk < 128, Nk = 1), Nq = Nk,
 both masks, one split, the automatic choice, more splits than tiles (clamped),
-a split whose keys some queries cannot see (empty partial), and wide score
-rows (Q x 8) so the running maximum moves between tiles and splits.
+both merge paths (a head's splits as one cluster merging in shared memory;
+more than 16 splits through the workspace and the merge kernel), a split whose
+keys some queries cannot see (empty partial), and wide score rows (Q x 8) so
+the running maximum moves between tiles and splits.
 Tolerances are the forward's: O max-abs 1e-2, lse max-abs 1e-3.
 """
 
@@ -35,6 +37,8 @@ CASES = [
     (1, 3, 7, 3000, 128, True, 0, "wide"),
     (2, 2, 1, 5000, 64, False, 7, "wide"),
     (1, 2, 6, 100, 128, True, 5, None),
+    (1, 2, 2, 4000, 128, True, 20, None),     # more than 16 splits: workspace + merge kernel
+    (3, 2, 1, 2000, 128, True, 12, "wide"),   # 12 splits: one cluster per head where launchable
 ]
 
 
@@ -87,13 +91,14 @@ def test_decode_workloads_sampled_heads(w):
 
 
 def test_workspace_rules():
-    q, k, v = (t.cuda() for t in make_decode_inputs(1, 2, 1, 1000, 64, seed=3))
+    # 20 splits (more than a cluster takes) of a 4000-key cache (32 tiles): the workspace path
+    q, k, v = (t.cuda() for t in make_decode_inputs(1, 2, 1, 4000, 64, seed=3))
     o = torch.empty_like(q)
     lse = torch.empty((1, 2, 1), device="cuda", dtype=torch.float32)
     s = torch.cuda.current_stream().cuda_stream
-    need = fa.fa_fwd_splitkv_workspace_size(1, 2, 1, 1000, 64, 4)
+    need = fa.fa_fwd_splitkv_workspace_size(1, 2, 1, 4000, 64, 20)
     assert need > 0
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 2, 1, 1000, 64, 0.125, 1, 4)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 2, 1, 4000, 64, 0.125, 1, 20)
     assert fa.fa_fwd_splitkv(*args, None, 0, s) == fa.FA_ERR_WORKSPACE
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need - 256, s) == fa.FA_ERR_WORKSPACE
