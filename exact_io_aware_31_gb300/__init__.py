@@ -20,7 +20,7 @@ import ctypes
 import os
 
 __all__ = [
-    "LIB_PATH", "FaError", "load_library", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
+    "LIB_PATH", "FaError", "load_library", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_deterministic",
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "decode_forward",
     "fa_get_device_status", "fa_status_string", "forward", "backward", "EXPORTED_SYMBOLS",
@@ -38,7 +38,8 @@ FA_ERR_CUDA = 4
 FA_ERR_DEVICE_TIMEOUT = 5
 FA_ERR_INTERNAL = 6
 
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_dkdv",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_deterministic", "fa_bwd_preprocess",
+                    "fa_bwd_dkdv",
                     "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
                     "fa_get_device_status", "fa_status_string")
 
@@ -71,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_bwd_deterministic.restype = i
+    lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_bwd_preprocess.restype = i
     lib.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp, sz, vp]
     lib.fa_bwd_dkdv.restype = i
@@ -104,6 +107,12 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspa
            stream) -> int:
     return load_library().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace,
                                  workspace_bytes, stream)
+
+
+def fa_bwd_deterministic(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes,
+                         stream) -> int:
+    return load_library().fa_bwd_deterministic(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal,
+                                               workspace, workspace_bytes, stream)
 
 
 def fa_bwd_preprocess(o, dout, lse, B, H, N, d, workspace, workspace_bytes, stream) -> int:
@@ -177,8 +186,11 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
     return o, l
 
 
-def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, grads=None, stream=None):
-    """Gradients ``(dq, dk, dv)`` of ``sum(O * dout)``; ``o`` and ``lse`` from :func:`forward`."""
+def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, grads=None, stream=None,
+             deterministic=False):
+    """Gradients ``(dq, dk, dv)`` of ``sum(O * dout)``; ``o`` and ``lse`` from :func:`forward`.
+
+    ``deterministic=True`` uses ``fa_bwd_deterministic`` (bitwise reproducible, slower)."""
     import torch
     B, H, N, d = q.shape
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
@@ -194,11 +206,12 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, gr
     dq, dk, dv = grads
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(t, name, (B, H, N, d), torch.bfloat16)
-    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
-                workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    fn = fa_bwd_deterministic if deterministic else fa_bwd
+    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
     if st != FA_OK:
-        raise FaError(st, "fa_bwd")
+        raise FaError(st, "fa_bwd_deterministic" if deterministic else "fa_bwd")
     return dq, dk, dv
 
 

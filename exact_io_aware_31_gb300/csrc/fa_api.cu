@@ -399,6 +399,25 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   return cuda_status(launch_bwd_conv(a, stream));
 }
 
+extern "C" int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                    const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                    float scale, int causal, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+  BwdLaunch a;
+  CUtensorMap maps[7];
+  int st = prepare_bwd(a, maps, kNeedQKV | kNeedO | kNeedDout | kNeedLse | kNeedDq | kNeedDkDv, q, k, v, o, dout,
+                       lse, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  a.with_dq = 0;  // dK / dV kernel without dQ; dQ from the query-outer kernel
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const int units = bwd_dq_units(a.BH, N);
+  a.dq_grid = units < dev->sms ? units : dev->sms;
+  if ((st = cuda_status(launch_bwd_pre(a, stream))) != FA_OK) return st;
+  if ((st = cuda_status(launch_bwd_main(a, stream))) != FA_OK) return st;
+  return cuda_status(launch_bwd_dq(a, stream));
+}
+
 extern "C" int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   BwdLaunch a;

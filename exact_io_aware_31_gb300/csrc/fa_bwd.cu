@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restric
                                                   const __nv_bfloat16* __restrict__ dout,
                                                   const float* __restrict__ lse, float* __restrict__ lse2,
                                                   float* __restrict__ dsum, float* __restrict__ dq_acc, int BH,
-                                                  int N, int Npad) {
+                                                  int N, int Npad, int zero_dq) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = threadIdx.x % 32;
@@ -121,9 +121,11 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __nv_bfloat16* __restric
         acc = fmaf(a.x, b.x, acc);
         acc = fmaf(a.y, b.y, acc);
       }
-      float4* z = reinterpret_cast<float4*>(dq_acc + base);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (zero_dq) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + base);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
     for (int off = kLanesPerRow / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -150,11 +152,13 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_conv(const float* __restrict__ 
 }
 
 // ------------------------------------------------------------- main kernel --
-template <int D>
+// DQ = false builds the dK / dV-only variant of the deterministic backward
+// (dQ then comes from fa_bwd_dq, with no reductions at all).
+template <int D, bool DQ = true>
 struct BwdCfg {
   static constexpr int kStages = 2;                   // Q / dO (+ lse2 / D rows) ring
   static constexpr int kKvStages = (D == 64) ? 2 : 1; // K / V buffers (next unit prefetch)
-  static constexpr bool kDqAliasesDp = (D == 128);    // no spare TMEM columns at d = 128
+  static constexpr bool kDqAliasesDp = DQ && (D == 128);  // no spare TMEM columns at d = 128
   // At d = 128 the partial is computed transposed, dQ^T = K^T dS^T (TMEM lanes =
   // head dimension), so a warp's reductions cover contiguous 128-byte rows of
   // the accumulator; at d = 64 (M = 64 is not used) it is dQ = dS K, staged in
@@ -167,7 +171,7 @@ struct BwdCfg {
   // never waits on them); d = 128: the compute warpgroups drain it with
   // coalesced reductions (FA_BWD_DQ_WARPGROUP selects the dedicated
   // warpgroup there too; it measured slower).
-  static constexpr bool kDqWarpgroup = !kDqTransposed || (FA_BWD_DQ_WARPGROUP != 0);
+  static constexpr bool kDqWarpgroup = DQ && (!kDqTransposed || (FA_BWD_DQ_WARPGROUP != 0));
   // d = 64: dK / dV leave through the dS buffer (free once the unit's last
   // MMAs are done) as two 64-column boxes with TMA stores; at d = 128 they
   // do not fit there and each thread stores its own row.
@@ -187,7 +191,7 @@ struct BwdCfg {
   static constexpr int kColDP = 128;  // dP^T
   static constexpr int kColDV = 256;
   static constexpr int kColDK = 256 + D;
-  static constexpr int kColDQ = kDqAliasesDp ? kColDP : 256 + 2 * D;
+  static constexpr int kColDQ = !DQ ? 0 : kDqAliasesDp ? kColDP : 256 + 2 * D;
   // d = 64 with FA_BWD_DS_TMEM: dS^T also packed as bf16 pairs in the last 64
   // columns, so dK takes its A operand from TMEM instead of shared memory
   // (d = 128 has no room).  Measured slower (the extra TMEM store sits on the
@@ -203,12 +207,12 @@ struct BwdCfg {
   // those two to finish reading dS(i).  At d = 128 the dQ^T partial occupies
   // the dP^T columns, so dP^T(i+1) waits until dQ^T(i) has been drained.
   static constexpr bool kEarlyDp = !kDqAliasesDp;
-  static constexpr int kDsBufs = kEarlyDp ? 2 : 1;
+  static constexpr int kDsBufs = (kEarlyDp && D == 64) ? 2 : 1;  // no room for a second one at d = 128
   static constexpr int kDsBytes = 2 * kSwzBlockBytes;              // 128 x 128 bf16 dS^T, two swizzle blocks
   static constexpr int kOffDS = kOffDO + kStages * kTileBytes;    // [kDsBufs]
   // d = 64: staging buffer of the dQ partial (128 rows x 64 fp32, as two
   // 128-byte-swizzled 32-column boxes) for the tensor reduce-add.
-  static constexpr int kDqStageBytes = kDqTransposed ? 0 : kTileRows * D * 4;
+  static constexpr int kDqStageBytes = (DQ && !kDqTransposed) ? kTileRows * D * 4 : 0;
   static constexpr int kOffDQS = kOffDS + kDsBufs * kDsBytes;
   static constexpr int kOffRow = kOffDQS + kDqStageBytes;        // [stages][lse2 128 | D 128] fp32
   static constexpr int kRowBytes = 2 * kTileRows * 4;
@@ -218,7 +222,7 @@ struct BwdCfg {
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kColDQ + D <= kTmemCols, "tensor memory budget");
+  static_assert(!DQ || kColDQ + D <= kTmemCols, "tensor memory budget");
   static_assert(!kDsTmem || (kColDST >= kColDQ + D && kColDST + 64 <= kTmemCols), "dS^T columns");
 };
 
@@ -255,8 +259,8 @@ __device__ __forceinline__ uint32_t pt_col(int k) {
   return QC * (k / (QC / 16)) + 8 * (k % (QC / 16));
 }
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+template <int D, bool CAUSAL, bool DQ>
+__global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_dqacc, const __grid_constant__ CUtensorMap tm_dk,
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 const float* __restrict__ dsum, float* __restrict__ dq_acc,
                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int N, int Npad, float c2,
                 float scale, int* status) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, DQ>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
   uint8_t* sm = smem_raw;
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             issue_dp(st2);
             tr(13);
           }
-          if (!C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
+          if (DQ && !C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
           tr(16);
           if (!ok) break;
           tc_fence_after();
@@ -555,16 +559,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               mma_ss(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
                      sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
           }
+          if (DQ) {
 #pragma unroll
-          for (int k = 0; k < kTileRows / 16; ++k) {
-            const uint64_t dsd = sdesc(dsb + k * 2048, kSwzBlockBytes, 1024);  // dS^T, 16 keys
-            const uint64_t kd = sdesc(k_s + k * 2048, kSwzBlockBytes, 1024);   // K, 16 keys
-            if (C::kDqTransposed)
-              mma_ss(tbase + C::kColDQ, kd, dsd, kIdQ, k > 0);  // dQ^T = K^T dS^T
-            else
-              mma_ss(tbase + C::kColDQ, dsd, kd, kIdQ, k > 0);  // dQ = dS K
+            for (int k = 0; k < kTileRows / 16; ++k) {
+              const uint64_t dsd = sdesc(dsb + k * 2048, kSwzBlockBytes, 1024);  // dS^T, 16 keys
+              const uint64_t kd = sdesc(k_s + k * 2048, kSwzBlockBytes, 1024);   // K, 16 keys
+              if (C::kDqTransposed)
+                mma_ss(tbase + C::kColDQ, kd, dsd, kIdQ, k > 0);  // dQ^T = K^T dS^T
+              else
+                mma_ss(tbase + C::kColDQ, dsd, kd, kIdQ, k > 0);  // dQ = dS K
+            }
+            mma_commit(dq_full);
           }
-          mma_commit(dq_full);
           mma_commit(db ? ds_empty2 : ds_empty);
           mma_commit(&qdo_empty[st]);
           ++dqcnt;
@@ -703,7 +709,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_arrive(p_full);
         tr(3);
         // ---- dQ partial of the previous query tile ----
-        if (!C::kDqWarpgroup) {
+        if (DQ && !C::kDqWarpgroup) {
           // dQ of the previous query tile: this unit's, or the last one of
           // the previous unit (deferred so the unit boundary does not wait).
           if (x > 0) {
@@ -779,7 +785,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
       if (!ok) break;
       // ---- dQ partial of the unit's last query tile ----
-      if (!C::kDqWarpgroup) {  // the unit's last dQ partial drains after P(0) of the next unit
+      if (DQ && !C::kDqWarpgroup) {  // the unit's last dQ partial drains after P(0) of the next unit
         pend_bh = u.bh;
         pend_qt = u.qtile(u.nq - 1);
       }
@@ -866,7 +872,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tr(7);
       if (aborted(abort_flag)) ok = false;
     }
-    if (ok && pend_qt >= 0) ok = drain_dq(pend_bh, pend_qt);
+    if (DQ && ok && pend_qt >= 0) ok = drain_dq(pend_bh, pend_qt);
     if (!ok) *abort_flag = 1;
     // dK / dV stores still in flight must finish before the CTA exits.
     if (C::kEpiTma && warp == 0 && lane == 0) tma_store_wait_all0();
@@ -970,10 +976,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DQ>
 static cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
-  using C = BwdCfg<D>;
-  auto kern = fa_bwd_main<D, CAUSAL>;
+  using C = BwdCfg<D, DQ>;
+  auto kern = fa_bwd_main<D, CAUSAL, DQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk,
@@ -988,15 +994,21 @@ cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream) {
   auto o = reinterpret_cast<const __nv_bfloat16*>(a.o);
   auto dout = reinterpret_cast<const __nv_bfloat16*>(a.dout);
   if (a.d == 64)
-    fa_bwd_pre<64><<<a.pre_grid, 256, 0, stream>>>(o, dout, a.lse, a.lse2, a.dsum, a.dq_acc, a.BH, a.N, a.Npad);
+    fa_bwd_pre<64><<<a.pre_grid, 256, 0, stream>>>(o, dout, a.lse, a.lse2, a.dsum, a.dq_acc, a.BH, a.N, a.Npad,
+                                                   a.with_dq);
   else
-    fa_bwd_pre<128><<<a.pre_grid, 256, 0, stream>>>(o, dout, a.lse, a.lse2, a.dsum, a.dq_acc, a.BH, a.N, a.Npad);
+    fa_bwd_pre<128><<<a.pre_grid, 256, 0, stream>>>(o, dout, a.lse, a.lse2, a.dsum, a.dq_acc, a.BH, a.N, a.Npad,
+                                                    a.with_dq);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
-  if (a.d == 64) return a.causal ? launch_main_t<64, true>(a, stream) : launch_main_t<64, false>(a, stream);
-  return a.causal ? launch_main_t<128, true>(a, stream) : launch_main_t<128, false>(a, stream);
+  if (a.with_dq) {
+    if (a.d == 64) return a.causal ? launch_main_t<64, true, true>(a, stream) : launch_main_t<64, false, true>(a, stream);
+    return a.causal ? launch_main_t<128, true, true>(a, stream) : launch_main_t<128, false, true>(a, stream);
+  }
+  if (a.d == 64) return a.causal ? launch_main_t<64, true, false>(a, stream) : launch_main_t<64, false, false>(a, stream);
+  return a.causal ? launch_main_t<128, true, false>(a, stream) : launch_main_t<128, false, false>(a, stream);
 }
 
 cudaError_t launch_bwd_conv(const BwdLaunch& a, cudaStream_t stream) {

@@ -44,6 +44,8 @@ struct BwdLaunch {
   int* status;
   int grid;
   int pre_grid;
+  int with_dq = 1;  // 0: deterministic backward (dK/dV kernel without dQ, dQ from fa_bwd_dq)
+  int dq_grid = 0;
 };
 
 // Split-KV forward (decode): Nq <= 8 queries per head against Nk keys.
@@ -70,6 +72,8 @@ int decode_max_clusters(int d, int nq, int causal, int cluster);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd_conv(const BwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t stream);
+int bwd_dq_units(int BH, int N);
 int fwd_units(int BH, int N);
 int bwd_units(int BH, int N);
 

@@ -142,6 +142,20 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Deterministic backward (bitwise the same on every run): the same arguments,
+ * workspace and results as fa_bwd, without any reduction between CTAs.
+ * [L] Step 3 and [T] "The backward pass: recompute instead of read": the
+ * gradients are rebuilt tile by tile in the two loop orders, key tiles outer
+ * for dK and dV (as in fa_bwd, minus dQ) and query tiles outer for dQ, which
+ * accumulates in tensor memory in a fixed order and is written once.  Three
+ * launches on `stream`: preprocess (D and lse * log2 e), the dK / dV kernel,
+ * the dQ kernel.  Slower than fa_bwd (S and P are rebuilt twice).
+ */
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * The three launches of fa_bwd as separate calls, for callers that schedule
  * or time them individually.  Running them in this order on one stream with
  * one workspace is exactly fa_bwd; arguments mean the same as there.

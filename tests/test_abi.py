@@ -143,3 +143,15 @@ def test_splitkv_workspace_size_of_invalid_sizes_is_zero(lib):
     assert fa.fa_fwd_splitkv_workspace_size(1, 1, 9, 100, 64, 0) == 0     # Nq > 8
     assert fa.fa_fwd_splitkv_workspace_size(1, 1, 1, 100, 96, 0) == 0     # d = 96
     assert fa.fa_fwd_splitkv_workspace_size(0, 1, 1, 100, 64, 0) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(dq=None), fa.FA_ERR_INVALID_ARG),
+    (dict(workspace=None), fa.FA_ERR_WORKSPACE),
+])
+def test_bwd_deterministic_validation(lib, kw, code):
+    args = dict(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, B=1, H=1, N=16, d=64, scale=0.125,
+                causal=1, workspace=A, workspace_bytes=1 << 30, stream=None)
+    args.update(kw)
+    assert fa.fa_bwd_deterministic(**args) == code
