@@ -21,6 +21,7 @@ import os
 
 __all__ = [
     "LIB_PATH", "FaError", "load_library", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_deterministic",
+    "fa_fwd_dropout", "fa_bwd_dropout",
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "decode_forward",
     "fa_get_device_status", "fa_status_string", "forward", "backward", "EXPORTED_SYMBOLS",
@@ -38,7 +39,8 @@ FA_ERR_CUDA = 4
 FA_ERR_DEVICE_TIMEOUT = 5
 FA_ERR_INTERNAL = 6
 
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_deterministic", "fa_bwd_preprocess",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_deterministic", "fa_fwd_dropout",
+                    "fa_bwd_dropout", "fa_bwd_preprocess",
                     "fa_bwd_dkdv",
                     "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
                     "fa_get_device_status", "fa_status_string")
@@ -72,6 +74,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+    u64, u32 = ctypes.c_ulonglong, ctypes.c_uint
+    lib.fa_fwd_dropout.restype = i
+    lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u32, vp]
+    lib.fa_bwd_dropout.restype = i
+    lib.fa_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u32, vp, sz, vp]
     lib.fa_bwd_deterministic.restype = i
     lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_bwd_preprocess.restype = i
@@ -107,6 +114,16 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspa
            stream) -> int:
     return load_library().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace,
                                  workspace_bytes, stream)
+
+
+def fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, scale, causal, p_drop, seed, offset, stream) -> int:
+    return load_library().fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, scale, causal, p_drop, seed, offset, stream)
+
+
+def fa_bwd_dropout(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, p_drop, seed, offset, workspace,
+                   workspace_bytes, stream) -> int:
+    return load_library().fa_bwd_dropout(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, p_drop, seed,
+                                         offset, workspace, workspace_bytes, stream)
 
 
 def fa_bwd_deterministic(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes,

@@ -310,6 +310,60 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   return FA_OK;
 }
 
+namespace fa {
+namespace {
+
+// Dropout parameters of the C ABI -> kernel form; FA_ERR_INVALID_ARG unless 0 <= p < 1.
+int drop_params(float p_drop, unsigned long long seed, unsigned int offset, DropParams* out) {
+  if (!std::isfinite(p_drop) || p_drop < 0.f || p_drop >= 1.f) return FA_ERR_INVALID_ARG;
+  const double t = std::nearbyint((double)p_drop * 4294967296.0);
+  out->thr = t >= 4294967295.0 ? 0xFFFFFFFFu : (uint32_t)t;
+  out->k0 = (uint32_t)(seed & 0xFFFFFFFFull);
+  out->k1 = (uint32_t)(seed >> 32);
+  out->offset = offset;
+  out->inv_keep = (float)(1.0 / (1.0 - (double)p_drop));
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                              int d, float scale, int causal, float p_drop, unsigned long long seed,
+                              unsigned int offset, cudaStream_t stream) {
+  DropParams dp;
+  int st = drop_params(p_drop, seed, offset, &dp);
+  if (st != FA_OK) return st;
+  if ((st = check_sizes(B, H, N, d, scale, causal)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (make_map(&tq, q, BH, N, d) || make_map(&tk, k, BH, N, d) || make_map(&tv, v, BH, N, d)) return FA_ERR_CUDA;
+  FwdLaunch a;
+  a.tm_q = &tq;
+  a.tm_k = &tk;
+  a.tm_v = &tv;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.c2 = log2_scale(scale);
+  a.status = dev->status;
+  a.dropout = 1;
+  a.drop = dp;
+  const int units = fwd_units(BH, N);
+  a.grid = units < dev->sms ? units : dev->sms;
+  if (launch_fwd(a, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_sizes(B, H, N, d, 1.0f, 0) != FA_OK) return 0;
   return workspace_layout(B, H, N, d).total;
@@ -394,6 +448,25 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   int st = prepare_bwd(a, maps, kNeedQKV | kNeedO | kNeedDout | kNeedLse | kNeedDq | kNeedDkDv, q, k, v, o, dout,
                        lse, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes);
   if (st != FA_OK) return st;
+  if ((st = cuda_status(launch_bwd_pre(a, stream))) != FA_OK) return st;
+  if ((st = cuda_status(launch_bwd_main(a, stream))) != FA_OK) return st;
+  return cuda_status(launch_bwd_conv(a, stream));
+}
+
+extern "C" int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                              int causal, float p_drop, unsigned long long seed, unsigned int offset,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  DropParams dp;
+  int st = drop_params(p_drop, seed, offset, &dp);
+  if (st != FA_OK) return st;
+  BwdLaunch a;
+  CUtensorMap maps[7];
+  st = prepare_bwd(a, maps, kNeedQKV | kNeedO | kNeedDout | kNeedLse | kNeedDq | kNeedDkDv, q, k, v, o, dout, lse, dq,
+                   dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  a.dropout = 1;
+  a.drop = dp;
   if ((st = cuda_status(launch_bwd_pre(a, stream))) != FA_OK) return st;
   if ((st = cuda_status(launch_bwd_main(a, stream))) != FA_OK) return st;
   return cuda_status(launch_bwd_conv(a, stream));

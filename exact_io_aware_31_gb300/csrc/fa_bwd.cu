@@ -50,6 +50,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_common.cuh"
+#include "fa_dropout.cuh"
 #include "fa_kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -259,7 +260,9 @@ __device__ __forceinline__ uint32_t pt_col(int k) {
   return QC * (k / (QC / 16)) + 8 * (k % (QC / 16));
 }
 
-template <int D, bool CAUSAL, bool DQ>
+// DROP: gradients of the forward with dropout (fa_dropout.cuh): dV takes
+// P o M / (1 - p), and dS = P o (dP o M / (1 - p) - D).
+template <int D, bool CAUSAL, bool DQ, bool DROP>
 __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
                 const __grid_constant__ CUtensorMap tm_dv, const float* __restrict__ lse2,
                 const float* __restrict__ dsum, float* __restrict__ dq_acc,
                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int N, int Npad, float c2,
-                float scale, int* status) {
+                float scale, DropParams dp, int* status) {
   using C = BwdCfg<D, DQ>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
@@ -670,6 +673,28 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         tc_fence_after();
         uint32_t pk[kQC / 2];  // this warpgroup's P^T row, bf16 pairs (reused for dS)
         uint32_t svall[kQC];   // the whole S^T row piece: every load in flight, one wait
+        // DROP: keep bit of (query qbase + c, this thread's key) for c < kQC.  A
+        // generator call covers four consecutive keys, which sit in four
+        // consecutive lanes: lane s of a group computes the call for query
+        // qb + s and the group exchanges words in three shuffles, so that
+        // each lane ends with its own key's word for the four queries.
+        uint64_t keep = ~0ull;
+        if (DROP) {
+          keep = 0ull;
+          const int s4 = lane & 3, g4 = lane & ~3;
+#pragma unroll 4
+          for (int b4 = 0; b4 < kQC / 4; ++b4) {
+            const uint4 w = philox4x32_10((uint32_t)(kr >> 2), (uint32_t)(qbase + 4 * b4 + s4), (uint32_t)u.bh,
+                                          dp.offset, dp.k0, dp.k1);
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int want = (s4 - rr) & 3;  // the word the lane reading from this one needs
+              const uint32_t val = want == 0 ? w.x : want == 1 ? w.y : want == 2 ? w.z : w.w;
+              const uint32_t got = __shfl_sync(0xffffffffu, val, g4 | ((s4 + rr) & 3));
+              if (got >= dp.thr) keep |= 1ull << (4 * b4 + ((s4 + rr) & 3));
+            }
+          }
+        }
 #pragma unroll
         for (int c = 0; c < kQC / 32; ++c) tmem_ld32(t_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&svall[32 * c]));
         tmem_wait_ld();
@@ -700,10 +725,23 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
             }
             pk[16 * c + e] = key_ok ? pack_bf16x2(p0, p1) : 0u;
           }
+          if (DROP) {  // the dV operand: surviving probabilities times 1 / (1 - p), over this chunk's S^T columns
+            uint32_t pt[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[16 * c + e]));
+              const int bit = 32 * c + 2 * e;
+              pt[e] = pack_bf16x2(((keep >> bit) & 1) ? pf.x * dp.inv_keep : 0.f,
+                                  ((keep >> (bit + 1)) & 1) ? pf.y * dp.inv_keep : 0.f);
+            }
+            tmem_st16(t_s + 16 * c, pt);
+          }
         }
         // This warpgroup's S^T columns are fully read: P^T goes over the first half.
+        if (!DROP) {
 #pragma unroll
-        for (int c = 0; c < kQC / 32; ++c) tmem_st16(t_s + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
+          for (int c = 0; c < kQC / 32; ++c) tmem_st16(t_s + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_full);
@@ -758,8 +796,13 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
               const int idx = 4 * m + e;  // pair index within the half
               const uint64_t nd = (e == 0) ? nd01.x : (e == 1) ? nd01.y : (e == 2) ? nd23.x : nd23.y;
               const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[idx]));
-              const uint64_t t =
-                  f2_add(f2_pack(__uint_as_float(dpv[8 * mm + 2 * e]), __uint_as_float(dpv[8 * mm + 2 * e + 1])), nd);
+              float dp0 = __uint_as_float(dpv[8 * mm + 2 * e]), dp1 = __uint_as_float(dpv[8 * mm + 2 * e + 1]);
+              if (DROP) {  // dP o M / (1 - p)
+                const int bit = 2 * idx;
+                dp0 = ((keep >> bit) & 1) ? dp0 * dp.inv_keep : 0.f;
+                dp1 = ((keep >> (bit + 1)) & 1) ? dp1 * dp.inv_keep : 0.f;
+              }
+              const uint64_t t = f2_add(f2_pack(dp0, dp1), nd);
               float d0, d1;
               f2_unpack(f2_mul(f2_pack(pf.x, pf.y), t), d0, d1);
               dsk[e] = pack_bf16x2(d0, d1);
@@ -976,17 +1019,17 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool DQ>
+template <int D, bool CAUSAL, bool DQ, bool DROP = false>
 static cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
   using C = BwdCfg<D, DQ>;
-  auto kern = fa_bwd_main<D, CAUSAL, DQ>;
+  auto kern = fa_bwd_main<D, CAUSAL, DQ, DROP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk,
                                                        *a.tm_dv, a.lse2,
                                                        a.dsum, a.dq_acc, reinterpret_cast<__nv_bfloat16*>(a.dk),
                                                        reinterpret_cast<__nv_bfloat16*>(a.dv), a.BH, a.N, a.Npad,
-                                                       a.c2, a.scale, a.status);
+                                                       a.c2, a.scale, a.drop, a.status);
   return cudaGetLastError();
 }
 
@@ -1003,6 +1046,11 @@ cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
+  if (a.dropout) {  // the fused backward only
+    if (a.d == 64)
+      return a.causal ? launch_main_t<64, true, true, true>(a, stream) : launch_main_t<64, false, true, true>(a, stream);
+    return a.causal ? launch_main_t<128, true, true, true>(a, stream) : launch_main_t<128, false, true, true>(a, stream);
+  }
   if (a.with_dq) {
     if (a.d == 64) return a.causal ? launch_main_t<64, true, true>(a, stream) : launch_main_t<64, false, true>(a, stream);
     return a.causal ? launch_main_t<128, true, true>(a, stream) : launch_main_t<128, false, true>(a, stream);

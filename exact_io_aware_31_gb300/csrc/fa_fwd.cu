@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_common.cuh"
+#include "fa_dropout.cuh"
 #include "fa_kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -115,11 +116,14 @@ __device__ __forceinline__ FwdUnit fwd_decode(int pos, int nqb, int N, int nkv_t
   return u;
 }
 
-template <int D, bool CAUSAL>
+// DROP: dropout on the probabilities (fa_dropout.cuh): the row sum l keeps
+// every probability, the P fed to P V keeps only the surviving ones, and the
+// epilogue scales O by 1 / (1 - p).
+template <int D, bool CAUSAL, bool DROP>
 __global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
-                  float* __restrict__ lse, int BH, int N, float c2, int* status) {
+                  float* __restrict__ lse, int BH, int N, float c2, DropParams dp, int* status) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
@@ -430,6 +434,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           uint32_t pk[16];
+          uint4 rw = make_uint4(0u, 0u, 0u, 0u);  // DROP: generator words of keys c .. c + 3
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c = 32 * h + 2 * i;
@@ -445,6 +450,13 @@ __global__ void __launch_bounds__(320, 1)
             ls[i & 3] = f2_add(ls[i & 3], p);
             float p0, p1;
             f2_unpack(p, p0, p1);
+            if (DROP) {  // one generator call per four keys: words (x, y) for an even pair, (z, w) for an odd one
+              if ((i & 1) == 0)
+                rw = philox4x32_10((uint32_t)((j * kTileRows + c) >> 2), (uint32_t)qi, (uint32_t)u.bh, dp.offset,
+                                   dp.k0, dp.k1);
+              if (((i & 1) ? rw.z : rw.x) < dp.thr) p0 = 0.f;
+              if (((i & 1) ? rw.w : rw.y) < dp.thr) p1 = 0.f;
+            }
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st16(t_s + 16 * h, pk);
@@ -473,7 +485,7 @@ __global__ void __launch_bounds__(320, 1)
       ++ocnt;
       if (!ok) break;
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      const float inv_l = (DROP ? dp.inv_keep : 1.f) / l_run;
       __nv_bfloat16* orow = out + ((size_t)u.bh * N + qi) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -507,21 +519,25 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DROP>
 static cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, DROP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v,
                                                        reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N,
-                                                       a.c2, a.status);
+                                                       a.c2, a.drop, a.status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
-  if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
-  return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+  if (a.dropout) {
+    if (a.d == 64) return a.causal ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);
+    return a.causal ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, false, true>(a, stream);
+  }
+  if (a.d == 64) return a.causal ? launch_fwd_t<64, true, false>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
+  return a.causal ? launch_fwd_t<128, true, false>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
 }
 
 int fwd_units(int BH, int N) { return BH * ((N + 2 * kTileRows - 1) / (2 * kTileRows)); }

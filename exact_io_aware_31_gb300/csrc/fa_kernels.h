@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 
+#include "fa_dropout.cuh"
+
 namespace fa {
 
 struct FwdLaunch {
@@ -18,6 +20,8 @@ struct FwdLaunch {
   float c2;  // scale * log2(e)
   int* status;
   int grid;
+  int dropout = 0;  // 1: dropout on the probabilities with `drop`
+  DropParams drop;
 };
 
 struct BwdLaunch {
@@ -46,6 +50,8 @@ struct BwdLaunch {
   int pre_grid;
   int with_dq = 1;  // 0: deterministic backward (dK/dV kernel without dQ, dQ from fa_bwd_dq)
   int dq_grid = 0;
+  int dropout = 0;  // 1: gradients of the forward with dropout `drop`
+  DropParams drop;
 };
 
 // Split-KV forward (decode): Nq <= 8 queries per head against Nk keys.

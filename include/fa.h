@@ -142,6 +142,31 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Forward and backward with dropout on the attention probabilities.  [T] "The
+ * backward pass: recompute instead of read": the forward keeps only the
+ * dropout generator state and the backward regenerates the mask from it.
+ *
+ *   p_drop  probability of dropping a probability, 0 <= p_drop < 1
+ *   seed    64-bit key of the counter-based generator (Philox4x32-10)
+ *   offset  fourth counter word (e.g. a step count, for a fresh mask)
+ *
+ * Element (b, h, query i, key j) is kept iff word (j mod 4) of
+ * Philox4x32-10(counter = (j / 4, i, b H + h, offset), key = seed) is at
+ * least round(p_drop 2^32); O = (P o M / (1 - p_drop)) V, lse is that of the
+ * undropped softmax.  fa_bwd_dropout takes the same p_drop, seed and offset
+ * and fa_bwd's other arguments and workspace, and returns the gradients of
+ * that forward.  Errors as fa_fwd / fa_bwd, plus FA_ERR_INVALID_ARG for
+ * p_drop outside [0, 1).
+ */
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   float scale, int causal, float p_drop, unsigned long long seed, unsigned int offset,
+                   cudaStream_t stream);
+int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, float p_drop,
+                   unsigned long long seed, unsigned int offset, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
+/*
  * Deterministic backward (bitwise the same on every run): the same arguments,
  * workspace and results as fa_bwd, without any reduction between CTAs.
  * [L] Step 3 and [T] "The backward pass: recompute instead of read": the

@@ -155,3 +155,10 @@ def test_bwd_deterministic_validation(lib, kw, code):
                 causal=1, workspace=A, workspace_bytes=1 << 30, stream=None)
     args.update(kw)
     assert fa.fa_bwd_deterministic(**args) == code
+
+
+@pytest.mark.parametrize("p", [-0.1, 1.0, 1.5, float("nan")])
+def test_dropout_rate_validation(lib, p):
+    assert fa.fa_fwd_dropout(A, A, A, A, A, 1, 1, 16, 64, 0.125, 0, p, 1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_dropout(A, A, A, A, A, A, A, A, A, 1, 1, 16, 64, 0.125, 0, p, 1, 0, A, 1 << 30,
+                             None) == fa.FA_ERR_INVALID_ARG
