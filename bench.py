@@ -92,7 +92,7 @@ KERNEL_SOURCES = {
     "fa_bwd_main": ["fa_bwd.cu"],
     "fa_bwd_dq_conv": ["fa_bwd.cu"],
 }
-DEVICE_HEADERS = ["fa_common.cuh", "sm103_ptx.cuh", "exp2_poly.h"]
+DEVICE_HEADERS = ["fa_common.cuh", "fa_dropout.cuh", "sm103_ptx.cuh", "exp2_poly.h"]
 
 
 def source_hash(kernel):
