@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     }
   } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    {  // whole warp, converged: waits are warp-wide, one elected lane issues
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T: both K-major over d
       constexpr uint32_t kIdKV = idesc_bf16(128, D, 0, 1);    // dV, dK: B (dO / Q) MN-major
       constexpr uint32_t kIdQ = idesc_bf16(128, C::kDqTransposed ? 128 : D, 1, 1);  // dQ / dQ^T: A, B MN-major
@@ -463,30 +463,30 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         auto issue_st = [&](int st) {  // S^T = K Q^T
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            mma_ss(tbase + C::kColS, sdesc(kmajor(k_s, k), 16, 1024),
+            mma_ss_w(tbase + C::kColS, sdesc(kmajor(k_s, k), 16, 1024),
                    sdesc(kmajor(q_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
-          mma_commit(s_full);
+          mma_commit_w(s_full);
         };
         auto issue_dp = [&](int st) {  // dP^T = V dO^T
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            mma_ss(tbase + C::kColDP, sdesc(kmajor(v_s, k), 16, 1024),
+            mma_ss_w(tbase + C::kColDP, sdesc(kmajor(v_s, k), 16, 1024),
                    sdesc(kmajor(do_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
-          mma_commit(dp_full);
+          mma_commit_w(dp_full);
         };
         tr(10);
-        ok = mbar_wait(&kv_full[kb], (ucnt / C::kKvStages) & 1, status);
+        ok = mbar_wait_warp(&kv_full[kb], (ucnt / C::kKvStages) & 1, status);
         tr(11);
         if (!ok) break;
         {
           const int st = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
-          ok = mbar_wait(&q_full[st], ph, status);
+          ok = mbar_wait_warp(&q_full[st], ph, status);
           if (!ok) break;
           tc_fence_after();
           issue_st(st);
           if (C::kEarlyDp) {
-            ok = mbar_wait(&do_full[st], ph, status);
+            ok = mbar_wait_warp(&do_full[st], ph, status);
             if (!ok) break;
             tc_fence_after();
             issue_dp(st);
@@ -500,8 +500,8 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           if (!C::kEarlyDp) {
             // dP^T(i) once dO(i) is in and the dQ^T partial sharing its columns is drained
             tr(12);
-            ok = mbar_wait(&do_full[st], ph, status);
-            if (ok) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
+            ok = mbar_wait_warp(&do_full[st], ph, status);
+            if (ok) ok = mbar_wait_warp(dq_empty, (dqcnt & 1) ^ 1, status);
             tr(18);
             if (!ok) break;
             tc_fence_after();
@@ -510,20 +510,20 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           }
           // dV += P^T dO  (A = P^T from TMEM, B = dO MN-major); the first of a unit
           // also waits until the previous unit's dK/dV have been read out.
-          ok = mbar_wait(p_full, pcnt & 1, status);
-          if (ok && x == 0) ok = mbar_wait(dkdv_empty, (ucnt & 1) ^ 1, status);
+          ok = mbar_wait_warp(p_full, pcnt & 1, status);
+          if (ok && x == 0) ok = mbar_wait_warp(dkdv_empty, (ucnt & 1) ^ 1, status);
           tr(14);
           ++pcnt;
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ts(tbase + C::kColDV, tbase + C::kColS + pt_col<C::kQCols>(k),
+            mma_ts_w(tbase + C::kColDV, tbase + C::kColS + pt_col<C::kQCols>(k),
                    sdesc(do_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
           tr(19);
           // S^T(i+1) as early as possible
           if (x + 1 < u.nq) {
-            ok = mbar_wait(&q_full[st2], ph2, status);
+            ok = mbar_wait_warp(&q_full[st2], ph2, status);
             tr(20);
             if (!ok) break;
             tc_fence_after();
@@ -531,20 +531,20 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           }
           // dS(i) in shared memory: [dP^T(i+1)], dK += dS^T Q, dQ_part = dS K
           tr(15);
-          ok = mbar_wait(ds_full, dscnt & 1, status);
+          ok = mbar_wait_warp(ds_full, dscnt & 1, status);
           const int db = dscnt % C::kDsBufs;
           ++dscnt;
           if (!ok) break;
           if (C::kEarlyDp && x + 1 < u.nq) {
             tr(12);
-            ok = mbar_wait(&do_full[st2], ph2, status);
+            ok = mbar_wait_warp(&do_full[st2], ph2, status);
             tr(18);
             if (!ok) break;
             tc_fence_after();
             issue_dp(st2);
             tr(13);
           }
-          if (DQ && !C::kDqAliasesDp) ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status);
+          if (DQ && !C::kDqAliasesDp) ok = mbar_wait_warp(dq_empty, (dqcnt & 1) ^ 1, status);
           tr(16);
           if (!ok) break;
           tc_fence_after();
@@ -553,13 +553,13 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
             // dK += dS^T Q with dS^T from TMEM (8 packed columns per 16 queries)
 #pragma unroll
             for (int k = 0; k < kTileRows / 16; ++k)
-              mma_ts(tbase + C::kColDK, tbase + C::kColDST + 8 * k,
+              mma_ts_w(tbase + C::kColDK, tbase + C::kColDST + 8 * k,
                      sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
-            mma_commit(dst_empty);  // dS^T in TMEM may be overwritten once dK(i) is done
+            mma_commit_w(dst_empty);  // dS^T in TMEM may be overwritten once dK(i) is done
           } else {
 #pragma unroll
             for (int k = 0; k < kTileRows / 16; ++k)
-              mma_ss(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
+              mma_ss_w(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
                      sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
           }
           if (DQ) {
@@ -568,26 +568,26 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
               const uint64_t dsd = sdesc(dsb + k * 2048, kSwzBlockBytes, 1024);  // dS^T, 16 keys
               const uint64_t kd = sdesc(k_s + k * 2048, kSwzBlockBytes, 1024);   // K, 16 keys
               if (C::kDqTransposed)
-                mma_ss(tbase + C::kColDQ, kd, dsd, kIdQ, k > 0);  // dQ^T = K^T dS^T
+                mma_ss_w(tbase + C::kColDQ, kd, dsd, kIdQ, k > 0);  // dQ^T = K^T dS^T
               else
-                mma_ss(tbase + C::kColDQ, dsd, kd, kIdQ, k > 0);  // dQ = dS K
+                mma_ss_w(tbase + C::kColDQ, dsd, kd, kIdQ, k > 0);  // dQ = dS K
             }
-            mma_commit(dq_full);
+            mma_commit_w(dq_full);
           }
-          mma_commit(db ? ds_empty2 : ds_empty);
-          mma_commit(&qdo_empty[st]);
+          mma_commit_w(db ? ds_empty2 : ds_empty);
+          mma_commit_w(&qdo_empty[st]);
           ++dqcnt;
           tr(17);
         }
         if (!ok) break;
-        mma_commit(dkdv_full);
-        mma_commit(&kv_empty[kb]);
+        mma_commit_w(dkdv_full);
+        mma_commit_w(&kv_empty[kb]);
         ++ucnt;
-        if (aborted(abort_flag)) ok = false;
+        if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
       }
       if (!ok) *abort_flag = 1;
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0, status);
+      mma_commit_w(mma_done);
+      mbar_wait_warp(mma_done, 0, status);
     }
   } else if (warp < C::kComputeWarps) {
     // ------------------------------------------------ compute warpgroups --

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     }
   } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    {  // whole warp, converged: waits are warp-wide, one elected lane issues
       constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // S, dP: A and B K-major over d
       constexpr uint32_t kIdQ = idesc_bf16(128, D, 0, 1);    // dQ += dS K: A from TMEM, B (K) MN-major
       auto kmajor = [](uint32_t base, int k) { return base + (k / 4) * kSwzBlockBytes + (k % 4) * 32; };
@@ -194,46 +194,46 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         const int qs = ucnt % C::kQStages;
         const uint32_t q_s = smem_addr(sm + C::kOffQ + qs * C::kTileBytes);
         const uint32_t do_s = smem_addr(sm + C::kOffDO + qs * C::kTileBytes);
-        if (!(ok = mbar_wait(&q_full[qs], (ucnt / C::kQStages) & 1, status))) break;
+        if (!(ok = mbar_wait_warp(&q_full[qs], (ucnt / C::kQStages) & 1, status))) break;
         for (int j = 0; j < nkv && ok; ++j, ++kvit) {
           const int ks = kvit % C::kKvStages;
           const uint32_t k_s = smem_addr(sm + C::kOffK + ks * C::kTileBytes);
           const uint32_t v_s = smem_addr(sm + C::kOffV + ks * C::kTileBytes);
-          if (!(ok = mbar_wait(&kv_full[ks], (kvit / C::kKvStages) & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&kv_full[ks], (kvit / C::kKvStages) & 1, status))) break;
           tc_fence_after();
           // S = Q K^T and dP = dO V^T (their TMEM columns were last read by
           // dQ of the previous key tile, issued before these)
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            mma_ss(tbase + C::kColS, sdesc(kmajor(q_s, k), 16, 1024), sdesc(kmajor(k_s, k), 16, 1024), kIdS, k > 0);
+            mma_ss_w(tbase + C::kColS, sdesc(kmajor(q_s, k), 16, 1024), sdesc(kmajor(k_s, k), 16, 1024), kIdS, k > 0);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            mma_ss(tbase + C::kColDP, sdesc(kmajor(do_s, k), 16, 1024), sdesc(kmajor(v_s, k), 16, 1024), kIdS,
+            mma_ss_w(tbase + C::kColDP, sdesc(kmajor(do_s, k), 16, 1024), sdesc(kmajor(v_s, k), 16, 1024), kIdS,
                    k > 0);
-          mma_commit(s_full);
+          mma_commit_w(s_full);
           // dQ += dS K_j, dS packed in TMEM over S
-          if (!(ok = mbar_wait(ds_full, dscnt & 1, status))) break;
+          if (!(ok = mbar_wait_warp(ds_full, dscnt & 1, status))) break;
           ++dscnt;
           // the first dQ MMA of a unit overwrites the columns: the previous
           // unit's dQ must have been read out
-          if (j == 0 && !(ok = mbar_wait(dq_empty, (dqcnt & 1) ^ 1, status))) break;
+          if (j == 0 && !(ok = mbar_wait_warp(dq_empty, (dqcnt & 1) ^ 1, status))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ts(tbase + C::kColDQ, tbase + C::kColS + dq_ds_col(k),
+            mma_ts_w(tbase + C::kColDQ, tbase + C::kColS + dq_ds_col(k),
                    sdesc(k_s + k * 2048, kSwzBlockBytes, 1024), kIdQ, (j > 0 || k > 0));
-          mma_commit(&kv_empty[ks]);
+          mma_commit_w(&kv_empty[ks]);
         }
         if (!ok) break;
-        mma_commit(&q_empty[qs]);
-        mma_commit(dq_full);
+        mma_commit_w(&q_empty[qs]);
+        mma_commit_w(dq_full);
         ++dqcnt;
         ++ucnt;
-        if (aborted(abort_flag)) ok = false;
+        if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
       }
       if (!ok) *abort_flag = 1;
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0, status);
+      mma_commit_w(mma_done);
+      mbar_wait_warp(mma_done, 0, status);
     }
   } else {
     // ------------------------------------------------ compute warpgroups --

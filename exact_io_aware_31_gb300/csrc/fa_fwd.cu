@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    {  // whole warp, converged: waits are warp-wide, one elected lane issues
       constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0, 0);  // S = Q K^T, both K-major
       constexpr uint32_t kIdescO = idesc_bf16(128, D, 0, 1);    // O += P V, V is MN-major
       const uint32_t q_s = smem_addr(sm + C::kOffQ);
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int t = 0; t < 2; ++t) {
           if (t >= u.nq || !ok) continue;
           qbuf[t] = t * C::kQBufs + qcnt[t] % C::kQBufs;
-          ok = mbar_wait(&B.q_full[qbuf[t]], (qcnt[t] / C::kQBufs) & 1, status);
+          ok = mbar_wait_warp(&B.q_full[qbuf[t]], (qcnt[t] / C::kQBufs) & 1, status);
           ++qcnt[t];
         }
         tr(11);
@@ -271,21 +271,21 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
-            mma_ss(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdescS,
+            mma_ss_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdescS,
                    k > 0);
           }
-          mma_commit(&B.s_full[t]);
+          mma_commit_w(&B.s_full[t]);
         };
         // prologue: S_t(0)
         {
           const int st = kv_it % C::kStages;
-          ok = mbar_wait(&B.k_full[st], (kv_it / C::kStages) & 1, status);
+          ok = mbar_wait_warp(&B.k_full[st], (kv_it / C::kStages) & 1, status);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (t < u.nq) issue_s(t, st);
-            if (t < u.nq && u.nkv(t) == 1) mma_commit(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+            if (t < u.nq && u.nkv(t) == 1) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
           }
         }
         for (int j = 0; j < u.nkv_max && ok; ++j) {
@@ -298,12 +298,12 @@ __global__ void __launch_bounds__(320, 1)
           if (t >= u.nq || !ok) continue;
             if (j >= u.nkv(t)) continue;
             tr(20 + t);
-            ok = mbar_wait(&B.p_full[t], pcnt[t] & 1, status);
+            ok = mbar_wait_warp(&B.p_full[t], pcnt[t] & 1, status);
             tr(22 + t);
             ++pcnt[t];
             if (!ok) break;
             if (!v_ready) {
-              ok = mbar_wait(&B.v_full[st], (it / C::kStages) & 1, status);
+              ok = mbar_wait_warp(&B.v_full[st], (it / C::kStages) & 1, status);
               if (!ok) break;
               v_ready = true;
             }
@@ -313,32 +313,32 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t va = v_s + st * C::kTileBytes;
 #pragma unroll
             for (int k = 0; k < kTileRows / 16; ++k)
-              mma_ts(tbase + C::kColO + D * t, tbase + C::kColS + 128 * t + k * 8,
+              mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColS + 128 * t + k * 8,
                      sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
             tr(28 + t);
             if (j + 1 < u.nkv(t)) {
               if (!k_next_ready) {
-                ok = mbar_wait(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
+                ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
                 if (!ok) break;
                 tc_fence_after();
                 k_next_ready = true;
               }
               tr(40 + t);
               issue_s(t, st_next);
-              if (j + 2 == u.nkv(t)) mma_commit(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+              if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
             } else {
-              mma_commit(&B.o_full[t]);
+              mma_commit_w(&B.o_full[t]);
             }
             tr(24 + t);
           }
-          if (ok) mma_commit(&B.kv_empty[st]);
+          if (ok) mma_commit_w(&B.kv_empty[st]);
         }
         kv_it += u.nkv_max;
-        if (aborted(abort_flag)) ok = false;
+        if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
       }
       if (!ok) *abort_flag = 1;
-      mma_commit(B.mma_done);
-      mbar_wait(B.mma_done, 0, status);
+      mma_commit_w(B.mma_done);
+      mbar_wait_warp(B.mma_done, 0, status);
     }
   } else {
     // -------------------------------------------------------------- softmax --
