@@ -13,14 +13,19 @@
 //   warps 4-7  softmax warpgroup for Q tile 1
 //   warp  8    TMA producer: Q tiles, then K_j / V_j into a STAGES-deep ring
 //   warp  9    TMEM owner and MMA issuer (one elected lane)
-// Tensor memory (512 columns): S_t at column 128 t (fp32 scores; P_t is
-// written back over its first 64 columns as packed bf16), O_t at 256 + D t.
-// Issue order on the tensor pipe alternates the two tiles:
+// Tensor memory (512 columns), d = 128: S_t at column 128 t (fp32 scores;
+// P_t is written back over its first 64 columns as packed bf16), O_t at
+// 256 + 128 t.  Issue order on the tensor pipe alternates the two tiles:
 //   S0(j) S1(j) | PV0(j) S0(j+1) | PV1(j) S1(j+1) | PV0(j+1) ...
 // so one warpgroup's softmax overlaps the other tile's two MMAs.  Because a
 // commit covers every earlier MMA of the issuing thread, the arrival that
 // publishes S_t(j+1) also proves PV_t(j) has finished: the softmax warpgroup
 // may then rescale O_t in place before it releases P_t(j+1).
+// d = 64: S_t at 128 t, P_t at 256 + 64 t, O_t at 384 + 64 t.  With P apart
+// from S the order per key tile is S0(j+1) S1(j+1) | PV0(j) | PV1(j): S_t(j+1)
+// only waits until the softmax has read S_t(j) into registers, so it runs
+// while P_t(j) is computed, and the softmax waits for PV_t(j) (a commit of its
+// own) before it rewrites P_t or rescales O_t.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -57,14 +62,21 @@ struct FwdCfg {
   static constexpr int kBlocks = D / 64;
   static constexpr int kThreads = 320;
   static constexpr int kTmemCols = 512;
-  static constexpr int kColS = 0;    // + 128 t
-  static constexpr int kColO = 256;  // + D t
+  // d = 64: P_t has TMEM columns of its own, so S_t(j+1) is issued as soon as
+  // the softmax has read S_t(j) and runs while P_t(j) is being computed.  At
+  // d = 128 two S and two O tiles fill the 512 columns and P_t is written over
+  // S_t, so S_t(j+1) waits for P_t(j) V_j.
+  static constexpr bool kSepP = (D == 64);
+  static constexpr int kColS = 0;                   // + 128 t
+  static constexpr int kColP = kSepP ? 256 : 0;     // + kPStride t
+  static constexpr int kPStride = kSepP ? 64 : 128;
+  static constexpr int kColO = kSepP ? 384 : 256;   // + D t
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQBufs * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  static constexpr int kNumBars = 2 * 2 * kQBufs + 3 * kStages + 3 * 2 + 1;
+  static constexpr int kNumBars = 2 * 2 * kQBufs + 3 * kStages + 5 * 2 + 1;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;
@@ -79,6 +91,8 @@ struct FwdBars {
   uint64_t* s_full;    // [2]
   uint64_t* p_full;    // [2]
   uint64_t* o_full;    // [2]
+  uint64_t* s_free;    // [2] (kSepP) the softmax has read S_t
+  uint64_t* pv_done;   // [2] (kSepP) P_t V_j has finished
   uint64_t* mma_done;  // [1]
 };
 
@@ -139,7 +153,9 @@ __global__ void __launch_bounds__(320, 1)
   B.s_full = B.kv_empty + C::kStages;
   B.p_full = B.s_full + 2;
   B.o_full = B.p_full + 2;
-  B.mma_done = B.o_full + 2;
+  B.s_free = B.o_full + 2;
+  B.pv_done = B.s_free + 2;
+  B.mma_done = B.pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
 
@@ -159,6 +175,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&B.s_full[t], 1);
       mbar_init(&B.p_full[t], 128);
       mbar_init(&B.o_full[t], 1);
+      mbar_init(&B.s_free[t], 128);
+      mbar_init(&B.pv_done[t], 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&B.k_full[s], 1);
@@ -247,6 +265,7 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t k_s = smem_addr(sm + C::kOffK);
       const uint32_t v_s = smem_addr(sm + C::kOffV);
       uint32_t qcnt[2] = {0, 0}, pcnt[2] = {0, 0};
+      uint32_t sis[2] = {0, 0};  // S_t issued so far (kSepP: each after the softmax read the previous one)
       uint32_t kv_it = 0;
       bool ok = true;
       Tracer tr(2);
@@ -266,7 +285,12 @@ __global__ void __launch_bounds__(320, 1)
         }
         tr(11);
         if (!ok) break;
-        auto issue_s = [&](int t, int st) {
+        auto issue_s = [&](int t, int st) -> bool {
+          if (C::kSepP) {  // S_t columns are free once the softmax has read the previous S_t
+            if (sis[t] > 0 && !mbar_wait_warp(&B.s_free[t], (sis[t] - 1) & 1, status)) return false;
+            tc_fence_after();
+          }
+          ++sis[t];
           const uint32_t qa = q_s + qbuf[t] * C::kTileBytes, ka = k_s + st * C::kTileBytes;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
@@ -275,6 +299,7 @@ __global__ void __launch_bounds__(320, 1)
                    k > 0);
           }
           mma_commit_w(&B.s_full[t]);
+          return true;
         };
         // prologue: S_t(0)
         {
@@ -284,10 +309,62 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (t < u.nq) issue_s(t, st);
-            if (t < u.nq && u.nkv(t) == 1) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+            if (t < u.nq && ok) ok = issue_s(t, st);
+            if (t < u.nq && ok && u.nkv(t) == 1) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
           }
+          if (!ok) break;
         }
+        if constexpr (C::kSepP) {
+          // Per key tile j: S_0(j+1), S_1(j+1) (each once the softmax has read
+          // S_t(j)), then P_t V_j for each tile once P_t(j) is written.
+          for (int j = 0; j < u.nkv_max && ok; ++j) {
+            const uint32_t it = kv_it + j;
+            const int st = it % C::kStages;
+            const int st_next = (it + 1) % C::kStages;
+            bool k_next_ready = false;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (t >= u.nq || j + 1 >= u.nkv(t) || !ok) continue;
+              if (!k_next_ready) {
+                ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                k_next_ready = true;
+              }
+              tr(40 + t);
+              ok = issue_s(t, st_next);
+              if (!ok) break;
+              if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+              tr(24 + t);
+            }
+            if (!ok) break;
+            bool v_ready = false;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (t >= u.nq || j >= u.nkv(t) || !ok) continue;
+              tr(20 + t);
+              ok = mbar_wait_warp(&B.p_full[t], pcnt[t] & 1, status);
+              tr(22 + t);
+              ++pcnt[t];
+              if (!ok) break;
+              if (!v_ready) {
+                ok = mbar_wait_warp(&B.v_full[st], (it / C::kStages) & 1, status);
+                if (!ok) break;
+                v_ready = true;
+              }
+              tr(26 + t);
+              tc_fence_after();
+              const uint32_t va = v_s + st * C::kTileBytes;
+#pragma unroll
+              for (int k = 0; k < kTileRows / 16; ++k)
+                mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t + k * 8,
+                         sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
+              mma_commit_w(&B.pv_done[t]);
+              tr(28 + t);
+            }
+            if (ok) mma_commit_w(&B.kv_empty[st]);
+          }
+        } else
         for (int j = 0; j < u.nkv_max && ok; ++j) {
           const uint32_t it = kv_it + j;
           const int st = it % C::kStages;
@@ -324,7 +401,8 @@ __global__ void __launch_bounds__(320, 1)
                 k_next_ready = true;
               }
               tr(40 + t);
-              issue_s(t, st_next);
+              ok = issue_s(t, st_next);
+              if (!ok) break;
               if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
             } else {
               mma_commit_w(&B.o_full[t]);
@@ -347,7 +425,8 @@ __global__ void __launch_bounds__(320, 1)
     const int r = quarter * 32 + lane; // row inside the tile
     const uint32_t t_s = tmem_lane_col(tbase, quarter * 32, C::kColS + 128 * t);
     const uint32_t t_o = tmem_lane_col(tbase, quarter * 32, C::kColO + D * t);
-    uint32_t scnt = 0, ocnt = 0;
+    const uint32_t t_p = tmem_lane_col(tbase, quarter * 32, C::kColP + C::kPStride * t);
+    uint32_t scnt = 0, ocnt = 0, pvcnt = 0;
     bool ok = true;
     Tracer tr(quarter == 0 ? t : -1);
     for (int round = 0; ok; ++round) {
@@ -375,6 +454,10 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld32(t_s + 32 * c, chunk);
         }
         tmem_wait_ld();
+        if (C::kSepP) {  // S_t(j) is in registers: the MMA warp may overwrite it with S_t(j+1)
+          tc_fence_before();
+          mbar_arrive(&B.s_free[t]);
+        }
         tr(3);
         float* s = reinterpret_cast<float*>(sv);
         const bool tail = (j == nkv_total - 1) && (N % kTileRows != 0);
@@ -395,12 +478,20 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 16; c < 128; c += 2) pm[(c / 2) & 7] = max3f(pm[(c / 2) & 7], s[c], s[c + 1]);
         const float mx = max3f(max3f(pm[0], pm[1], pm[2]), max3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
         const float mx2 = mx * c2;  // tile max in log2 units (c2 > 0)
+        if (C::kSepP && j > 0) {
+          // P_t(j - 1) V_{j-1} must be done: it reads the P_t columns about to
+          // be rewritten and accumulates into the O_t a rescale would touch.
+          ok = mbar_wait_warp(&B.pv_done[t], pvcnt & 1, status);
+          ++pvcnt;
+          if (!ok) break;
+          tc_fence_after();
+        }
         if (j == 0) {
           m_run = mx2;
         } else {
           const bool need = mx2 > m_run + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need)) {
-            // O_t is quiescent here (see header); rescale it and l by 2^(m_old - m_new).
+            // O_t is quiescent here (see header): rescale it and l by 2^(m_old - m_new).
             const float m_new = fmaxf(m_run, mx2);
             const float alpha = ex2(m_run - m_new);
             l_run *= alpha;
@@ -459,7 +550,7 @@ __global__ void __launch_bounds__(320, 1)
             }
             pk[i] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(t_s + 16 * h, pk);
+          tmem_st16(t_p + 16 * h, pk);
         }
         {
           const uint64_t t01 = f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3]));
@@ -480,9 +571,14 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
       // epilogue: O = O~ / l, lse = (m + log2 l) ln 2
       tr(6);
-      ok = mbar_wait_warp(&B.o_full[t], ocnt & 1, status);
+      if (C::kSepP) {
+        ok = mbar_wait_warp(&B.pv_done[t], pvcnt & 1, status);
+        ++pvcnt;
+      } else {
+        ok = mbar_wait_warp(&B.o_full[t], ocnt & 1, status);
+        ++ocnt;
+      }
       tr(7);
-      ++ocnt;
       if (!ok) break;
       tc_fence_after();
       const float inv_l = (DROP ? dp.inv_keep : 1.f) / l_run;
