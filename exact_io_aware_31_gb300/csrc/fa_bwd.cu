@@ -242,10 +242,9 @@ struct BwdUnit {
   }
 };
 
-__device__ __forceinline__ BwdUnit bwd_decode(int pos, int nkt, bool causal) {
+__device__ __forceinline__ BwdUnit bwd_decode(int pos, int BH, int nkt, bool causal, bool block_major) {
   BwdUnit u;
-  u.bh = pos / nkt;
-  u.j = pos - u.bh * nkt;  // ascending j = heaviest first under the causal mask
+  split_unit(pos, BH, nkt, block_major, u.bh, u.j);  // ascending j = heaviest first under the causal mask
   u.i0 = causal ? u.j : 0;
   u.nq = nkt - u.i0;
   u.rot = causal ? 0 : u.j;
@@ -306,6 +305,8 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
   const int nkt = (N + kTileRows - 1) / kTileRows;
   const int total_units = BH * nkt;
   const int grid = gridDim.x;
+  // d = 64 backward: slice-major measured faster at N = 4096 (L2 locality)
+  const bool block_major = D == 128 && block_major_order(CAUSAL, total_units, grid, N);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kKvStages; ++s) {
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
       bool ok = true;
       // K/V of the unit at `p` into buffer ucnt % kKvStages (waits for the buffer).
       auto issue_kv = [&](int p) -> bool {
-        const BwdUnit v = bwd_decode(p, nkt, CAUSAL);
+        const BwdUnit v = bwd_decode(p, BH, nkt, CAUSAL, block_major);
         const int kb = ucnt % C::kKvStages;
         tr(30);
         if (!mbar_wait(&kv_empty[kb], ((ucnt / C::kKvStages) & 1) ^ 1, status)) return false;
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         if (round * grid >= total_units) break;
         const int pos = snake_unit(round, blockIdx.x, grid);
         if (pos >= total_units) continue;
-        const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
+        const BwdUnit u = bwd_decode(pos, BH, nkt, CAUSAL, block_major);
         if (prefetched != pos && !(ok = issue_kv(pos))) break;
         prefetched = -1;
         // With two K/V buffers the next unit's copy goes out as soon as its
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         if (round * grid >= total_units) break;
         const int pos = snake_unit(round, blockIdx.x, grid);
         if (pos >= total_units) continue;
-        const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
+        const BwdUnit u = bwd_decode(pos, BH, nkt, CAUSAL, block_major);
         const int kb = ucnt % C::kKvStages;
         const uint32_t k_s = smem_addr(sm + C::kOffK + kb * C::kTileBytes);
         const uint32_t v_s = smem_addr(sm + C::kOffV + kb * C::kTileBytes);
@@ -653,7 +654,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
       if (round * grid >= total_units) break;
       const int pos = snake_unit(round, blockIdx.x, grid);
       if (pos >= total_units) continue;
-      const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
+      const BwdUnit u = bwd_decode(pos, BH, nkt, CAUSAL, block_major);
       const int kr = u.j * kTileRows + r;  // this thread's key
       const bool key_ok = kr < N;
       for (int x = 0; x < u.nq; ++x, ++qit) {
@@ -938,7 +939,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
       if (round * grid >= total_units) break;
       const int pos = snake_unit(round, blockIdx.x, grid);
       if (pos >= total_units) continue;
-      const BwdUnit u = bwd_decode(pos, nkt, CAUSAL);
+      const BwdUnit u = bwd_decode(pos, BH, nkt, CAUSAL, block_major);
       for (int x = 0; x < u.nq && ok; ++x) {
         tr(40);
         ok = mbar_wait_warp(dq_full, qcnt & 1, status);

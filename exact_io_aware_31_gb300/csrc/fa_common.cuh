@@ -28,6 +28,33 @@ __host__ __device__ inline int snake_unit(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
 
+// Unit order of the persistent schedules.  Slice-major (the units of one
+// (b, h) slice next to each other) keeps concurrently running units on the
+// same K/V in L2.  Block-major (block k, heaviest first, of every slice, then
+// block k + 1) balances the CTAs' totals when the causal mask makes units
+// unequal and each CTA runs only a few of them: for B = 1, H = 32, N = 4096
+// the busiest CTA's share drops from 1.19x to 1.03x of the mean.  Measured on
+// GB300, block-major wins for causal N >= 4096 with few units per CTA (B = 1,
+// H = 32, d = 128 forward: 0.130 -> 0.110 ms) and loses at N = 1024, where
+// locality matters more (B = 16, H = 16, d = 128: 0.089 -> 0.098 ms).
+#ifndef FA_BLOCK_MAJOR_MIN_N
+#define FA_BLOCK_MAJOR_MIN_N 4096  // tuning knob
+#endif
+__host__ __device__ inline bool block_major_order(bool causal, int total_units, int grid, int N) {
+  return causal && N >= FA_BLOCK_MAJOR_MIN_N && total_units < 16 * grid;
+}
+
+// Schedule position -> (slice bh, block index within the slice, 0 = first).
+__host__ __device__ inline void split_unit(int pos, int BH, int nblk, bool block_major, int& bh, int& blk) {
+  if (block_major) {
+    blk = pos / BH;
+    bh = pos - blk * BH;
+  } else {
+    bh = pos / nblk;
+    blk = pos - bh * nblk;
+  }
+}
+
 #ifdef __CUDACC__
 // Phase tracing, compiled in only with -DFA_TRACE (a separate build of the
 // library, never the default one).  Lane 0 of a traced role appends

@@ -104,10 +104,11 @@ struct FwdUnit {
   __device__ __forceinline__ int nkv(int t) const { return t ? nkv1 : nkv0; }
 };
 
-__device__ __forceinline__ FwdUnit fwd_decode(int pos, int nqb, int N, int nkv_total, bool causal) {
+__device__ __forceinline__ FwdUnit fwd_decode(int pos, int BH, int nqb, int N, int nkv_total, bool causal,
+                                              bool block_major) {
   FwdUnit u;
-  u.bh = pos / nqb;
-  const int r = pos - u.bh * nqb;
+  int r;
+  split_unit(pos, BH, nqb, block_major, u.bh, r);
   const int qb = causal ? (nqb - 1 - r) : r;  // heaviest first within a slice when causal
   u.q0 = qb * 2 * kTileRows;
   u.nq = (u.q0 + kTileRows < N) ? 2 : 1;
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(320, 1)
   const int nkv_total = (N + kTileRows - 1) / kTileRows;
   const int total_units = BH * nqb;
   const int grid = gridDim.x;
+  const bool block_major = block_major_order(CAUSAL, total_units, grid, N);
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < 2 * C::kQBufs; ++q) {
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(320, 1)
         const int pos = snake_unit(round, blockIdx.x, grid);
         if (round * grid >= total_units) break;
         if (pos >= total_units) continue;
-        const FwdUnit u = fwd_decode(pos, nqb, N, nkv_total, CAUSAL);
+        const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
         tr(30);
         #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__(320, 1)
         const int pos = snake_unit(round, blockIdx.x, grid);
         if (round * grid >= total_units) break;
         if (pos >= total_units) continue;
-        const FwdUnit u = fwd_decode(pos, nqb, N, nkv_total, CAUSAL);
+        const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
         tr(10);
         int qbuf[2] = {0, 0};  // Q buffer (t * kQBufs + b) each tile uses in this unit
         #pragma unroll
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(320, 1)
       const int pos = snake_unit(round, blockIdx.x, grid);
       if (round * grid >= total_units) break;
       if (pos >= total_units) continue;
-      const FwdUnit u = fwd_decode(pos, nqb, N, nkv_total, CAUSAL);
+      const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
       if (t >= u.nq) continue;
       const int qi = u.q0 + t * kTileRows + r;  // this thread's query row
       const int jdiag = (u.q0 + t * kTileRows) / kTileRows;
