@@ -530,23 +530,12 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
             tc_fence_after();
             issue_st(st2);
           }
-          // dS(i) in shared memory: [dP^T(i+1)], dK += dS^T Q, dQ_part = dS K
+          // dS(i) in shared memory: dK += dS^T Q (then the Q / dO slot is
+          // free: Q(i) has no later reader), [dP^T(i+1)], dQ_part = dS K
           tr(15);
           ok = mbar_wait_warp(ds_full, dscnt & 1, status);
           const int db = dscnt % C::kDsBufs;
           ++dscnt;
-          if (!ok) break;
-          if (C::kEarlyDp && x + 1 < u.nq) {
-            tr(12);
-            ok = mbar_wait_warp(&do_full[st2], ph2, status);
-            tr(18);
-            if (!ok) break;
-            tc_fence_after();
-            issue_dp(st2);
-            tr(13);
-          }
-          if (DQ && !C::kDqAliasesDp) ok = mbar_wait_warp(dq_empty, (dqcnt & 1) ^ 1, status);
-          tr(16);
           if (!ok) break;
           tc_fence_after();
           const uint32_t dsb = ds_s + db * C::kDsBytes;
@@ -563,6 +552,20 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
               mma_ss_w(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
                      sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
           }
+          mma_commit_w(&qdo_empty[st]);  // Q(i), dO(i) read for the last time: the producer may reload the slot
+          if (C::kEarlyDp && x + 1 < u.nq) {
+            tr(12);
+            ok = mbar_wait_warp(&do_full[st2], ph2, status);
+            tr(18);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(st2);
+            tr(13);
+          }
+          if (DQ && !C::kDqAliasesDp) ok = mbar_wait_warp(dq_empty, (dqcnt & 1) ^ 1, status);
+          tr(16);
+          if (!ok) break;
+          tc_fence_after();
           if (DQ) {
 #pragma unroll
             for (int k = 0; k < kTileRows / 16; ++k) {
@@ -576,7 +579,6 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
             mma_commit_w(dq_full);
           }
           mma_commit_w(db ? ds_empty2 : ds_empty);
-          mma_commit_w(&qdo_empty[st]);
           ++dqcnt;
           tr(17);
         }
