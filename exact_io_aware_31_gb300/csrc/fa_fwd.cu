@@ -8,11 +8,13 @@
 // streams K/V tiles past them, writing O once).
 //
 // Work unit: 256 query rows (two 128-row Q tiles, t = 0, 1) of one (b, h).
-// CTA roles (10 warps):
+// CTA roles (10 warps; 11 with PVW):
 //   warps 0-3  softmax warpgroup for Q tile 0   (thread = one query row)
 //   warps 4-7  softmax warpgroup for Q tile 1
 //   warp  8    TMA producer: Q tiles, then K_j / V_j into a STAGES-deep ring
-//   warp  9    TMEM owner and MMA issuer (one elected lane)
+//   warp  9    TMEM owner and MMA issuer (one elected lane); with PVW it
+//              issues the S MMAs only
+//   warp 10    (PVW, d = 64) issuer of the P V MMAs
 // Tensor memory (512 columns), d = 128: S_t at column 128 t (fp32 scores;
 // P_t is written back over its first 64 columns as packed bf16), O_t at
 // 256 + 128 t.  Issue order on the tensor pipe alternates the two tiles:
@@ -25,7 +27,12 @@
 // from S the order per key tile is S0(j+1) S1(j+1) | PV0(j) | PV1(j): S_t(j+1)
 // only waits until the softmax has read S_t(j) into registers, so it runs
 // while P_t(j) is computed, and the softmax waits for PV_t(j) (a commit of its
-// own) before it rewrites P_t or rescales O_t.
+// own) before it rewrites P_t or rescales O_t.  PVW (d = 64): the P V MMAs
+// come from a second issuing warp on another sub-partition (the S and P V
+// groups need no ordering between them), with K and V released separately;
+// one issuer cannot keep up with the softmax warpgroups that share its
+// sub-partition.  Measured faster for units of 8 or more key tiles and slower
+// for the short causal units of N <= 1024, so the launch picks it by shape.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -60,7 +67,6 @@ struct FwdCfg {
   static constexpr int kQBufs = (D == 128) ? 1 : 2;  // Q buffers per tile (next unit's Q prefetched at d = 64)
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
-  static constexpr int kThreads = 320;
   static constexpr int kTmemCols = 512;
   // d = 64: P_t has TMEM columns of its own, so S_t(j+1) is issued as soon as
   // the softmax has read S_t(j) and runs while P_t(j) is being computed.  At
@@ -71,12 +77,13 @@ struct FwdCfg {
   static constexpr int kColP = kSepP ? 256 : 0;     // + kPStride t
   static constexpr int kPStride = kSepP ? 64 : 128;
   static constexpr int kColO = kSepP ? 384 : 256;   // + D t
+  static constexpr int threads(bool pvw) { return pvw ? 352 : 320; }
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQBufs * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  static constexpr int kNumBars = 2 * 2 * kQBufs + 3 * kStages + 5 * 2 + 1;
+  static constexpr int kNumBars = 2 * 2 * kQBufs + 4 * kStages + 5 * 2 + 1;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;
@@ -87,7 +94,8 @@ struct FwdBars {
   uint64_t* q_empty;   // [2][kQBufs]
   uint64_t* k_full;    // [S]
   uint64_t* v_full;    // [S]
-  uint64_t* kv_empty;  // [S]
+  uint64_t* kv_empty;  // [S] (PVW: K_j read)
+  uint64_t* v_empty;   // [S] PVW: V_j read
   uint64_t* s_full;    // [2]
   uint64_t* p_full;    // [2]
   uint64_t* o_full;    // [2]
@@ -134,12 +142,13 @@ __device__ __forceinline__ FwdUnit fwd_decode(int pos, int BH, int nqb, int N, i
 // DROP: dropout on the probabilities (fa_dropout.cuh): the row sum l keeps
 // every probability, the P fed to P V keeps only the surviving ones, and the
 // epilogue scales O by 1 / (1 - p).
-template <int D, bool CAUSAL, bool DROP>
-__global__ void __launch_bounds__(320, 1)
+template <int D, bool CAUSAL, bool DROP, bool PVW>
+__global__ void __launch_bounds__(FwdCfg<D>::threads(PVW), 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ lse, int BH, int N, float c2, DropParams dp, int* status) {
   using C = FwdCfg<D>;
+  static_assert(!PVW || C::kSepP, "the P V warp needs P in columns of its own");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
   uint8_t* sm = smem_raw;
@@ -151,7 +160,8 @@ __global__ void __launch_bounds__(320, 1)
   B.k_full = bars + 4 * C::kQBufs;
   B.v_full = B.k_full + C::kStages;
   B.kv_empty = B.v_full + C::kStages;
-  B.s_full = B.kv_empty + C::kStages;
+  B.v_empty = B.kv_empty + C::kStages;
+  B.s_full = B.v_empty + C::kStages;
   B.p_full = B.s_full + 2;
   B.o_full = B.p_full + 2;
   B.s_free = B.o_full + 2;
@@ -184,8 +194,9 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&B.k_full[s], 1);
       mbar_init(&B.v_full[s], 1);
       mbar_init(&B.kv_empty[s], 1);
+      mbar_init(&B.v_empty[s], 1);
     }
-    mbar_init(B.mma_done, 1);
+    mbar_init(B.mma_done, PVW ? 2 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -239,6 +250,7 @@ __global__ void __launch_bounds__(320, 1)
           mbar_expect_tx(&B.k_full[st], C::kTileBytes);
           for (int kb = 0; kb < C::kBlocks; ++kb)
             tma_load_3d(kd + kb * kSwzBlockBytes, &tm_k, &B.k_full[st], kb * 64, j * kTileRows, u.bh);
+          if (PVW && !(ok = mbar_wait(&B.v_empty[st], ph ^ 1, status))) break;
           mbar_expect_tx(&B.v_full[st], C::kTileBytes);
           for (int kb = 0; kb < C::kBlocks; ++kb)
             tma_load_3d(vd + kb * kSwzBlockBytes, &tm_v, &B.v_full[st], kb * 64, j * kTileRows, u.bh);
@@ -316,7 +328,32 @@ __global__ void __launch_bounds__(320, 1)
           }
           if (!ok) break;
         }
-        if constexpr (C::kSepP) {
+        if constexpr (PVW) {
+          // Per key tile j: S_0(j+1), S_1(j+1), each once the softmax has read
+          // S_t(j); then K_j is released (its S MMAs were issued before).
+          for (int j = 0; j < u.nkv_max && ok; ++j) {
+            const uint32_t it = kv_it + j;
+            const int st = it % C::kStages;
+            const int st_next = (it + 1) % C::kStages;
+            bool k_next_ready = false;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (t >= u.nq || j + 1 >= u.nkv(t) || !ok) continue;
+              if (!k_next_ready) {
+                ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                k_next_ready = true;
+              }
+              tr(40 + t);
+              ok = issue_s(t, st_next);
+              if (!ok) break;
+              if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+              tr(24 + t);
+            }
+            if (ok) mma_commit_w(&B.kv_empty[st]);
+          }
+        } else if constexpr (C::kSepP) {
           // Per key tile j: S_0(j+1), S_1(j+1) (each once the softmax has read
           // S_t(j)), then P_t V_j for each tile once P_t(j) is written.
           for (int j = 0; j < u.nkv_max && ok; ++j) {
@@ -412,6 +449,52 @@ __global__ void __launch_bounds__(320, 1)
             tr(24 + t);
           }
           if (ok) mma_commit_w(&B.kv_empty[st]);
+        }
+        kv_it += u.nkv_max;
+        if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit_w(B.mma_done);
+      mbar_wait_warp(B.mma_done, 0, status);
+    }
+  } else if (PVW && warp == 10) {
+    // ------------------------------------------------------ P V issuer (PVW) --
+    {  // whole warp, converged: waits are warp-wide, one elected lane issues
+      constexpr uint32_t kIdescO = idesc_bf16(128, D, 0, 1);  // O += P V, V is MN-major
+      const uint32_t v_s = smem_addr(sm + C::kOffV);
+      uint32_t pcnt[2] = {0, 0};
+      uint32_t kv_it = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int pos = snake_unit(round, blockIdx.x, grid);
+        if (round * grid >= total_units) break;
+        if (pos >= total_units) continue;
+        const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
+        for (int j = 0; j < u.nkv_max && ok; ++j) {
+          const uint32_t it = kv_it + j;
+          const int st = it % C::kStages;
+          bool v_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t >= u.nq || j >= u.nkv(t) || !ok) continue;
+            ok = mbar_wait_warp(&B.p_full[t], pcnt[t] & 1, status);
+            ++pcnt[t];
+            if (!ok) break;
+            if (!v_ready) {
+              ok = mbar_wait_warp(&B.v_full[st], (it / C::kStages) & 1, status);
+              if (!ok) break;
+              v_ready = true;
+            }
+            tc_fence_after();
+            // O_t (+)= P_t V_j : A = P_t from TMEM (8 columns per 16 keys), B = V_j MN-major
+            const uint32_t va = v_s + st * C::kTileBytes;
+#pragma unroll
+            for (int k = 0; k < kTileRows / 16; ++k)
+              mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t + k * 8,
+                       sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
+            mma_commit_w(&B.pv_done[t]);
+          }
+          if (ok) mma_commit_w(&B.v_empty[st]);
         }
         kv_it += u.nkv_max;
         if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
@@ -617,25 +700,34 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool DROP>
+template <int D, bool CAUSAL, bool DROP, bool PVW = false>
 static cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, DROP>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, DROP, PVW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v,
+  kern<<<a.grid, C::threads(PVW), C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v,
                                                        reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N,
                                                        a.c2, a.drop, a.status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
-  if (a.dropout) {
-    if (a.d == 64) return a.causal ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);
-    return a.causal ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, false, true>(a, stream);
+// d = 64: the P V warp for units of 8 or more key tiles (N >= 1024), except
+// short causal units (causal N < 2048), where the single issuer measured faster.
+static bool use_pv_warp(const FwdLaunch& a) { return a.d == 64 && a.N >= 1024 && !(a.causal && a.N < 2048); }
+
+template <int D, bool DROP>
+static cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t stream) {
+  if constexpr (D == 64) {
+    if (use_pv_warp(a))
+      return a.causal ? launch_fwd_t<64, true, DROP, true>(a, stream) : launch_fwd_t<64, false, DROP, true>(a, stream);
   }
-  if (a.d == 64) return a.causal ? launch_fwd_t<64, true, false>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
-  return a.causal ? launch_fwd_t<128, true, false>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
+  return a.causal ? launch_fwd_t<D, true, DROP>(a, stream) : launch_fwd_t<D, false, DROP>(a, stream);
+}
+
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.dropout) return a.d == 64 ? launch_fwd_d<64, true>(a, stream) : launch_fwd_d<128, true>(a, stream);
+  return a.d == 64 ? launch_fwd_d<64, false>(a, stream) : launch_fwd_d<128, false>(a, stream);
 }
 
 int fwd_units(int BH, int N) { return BH * ((N + 2 * kTileRows - 1) / (2 * kTileRows)); }
