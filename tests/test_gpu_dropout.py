@@ -67,7 +67,9 @@ def test_keep_mask_bit_exact(d, p):
 
 
 CASES = [(1, 2, 256, 64, False, 0.1), (1, 2, 256, 128, True, 0.2), (2, 3, 300, 64, True, 0.5),
-         (1, 1, 129, 128, False, 0.3), (1, 2, 1000, 64, True, 0.1), (2, 1, 513, 128, True, 0.15)]
+         (1, 1, 129, 128, False, 0.3), (1, 2, 1000, 64, True, 0.1), (2, 1, 513, 128, True, 0.15),
+         # d = 64 forward with the second MMA issuer
+         (1, 1, 1100, 64, False, 0.2), (1, 1, 2100, 64, True, 0.1)]
 
 
 @pytest.mark.parametrize("B,H,N,d,causal,p", CASES,

@@ -29,6 +29,10 @@ SMALL = [
     (1, 1, 1, 64, False), (1, 1, 1, 128, True), (1, 1, 127, 64, True), (1, 1, 128, 128, False),
     (1, 1, 129, 64, False), (1, 1, 129, 128, True), (2, 3, 777, 64, False), (2, 3, 777, 128, True),
     (1, 2, 1000, 128, True), (1, 1, 300, 64, True), (3, 1, 513, 128, False), (1, 2, 640, 64, True),
+    # d = 64 forward with the second MMA issuer (non-causal N >= 1024, causal N >= 2048), ragged tails
+    (1, 1, 1100, 64, False), (1, 1, 2100, 64, True),
+    # causal N >= 4096 with few units per CTA: the block-major unit order
+    (1, 2, 4096, 128, True),
 ]
 
 
