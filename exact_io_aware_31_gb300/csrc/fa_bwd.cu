@@ -78,6 +78,17 @@ constexpr int kBwdPolyEvery = FA_BWD_POLY_EVERY;
 #ifndef FA_BWD_DS_TMEM
 #define FA_BWD_DS_TMEM 0
 #endif
+// Tuning knob (d = 128): issue the dQ^T reductions of the previous query tile
+// interleaved with the dS loop, eight per chunk of eight queries (1), or all
+// at once after the partial is read from TMEM (0).
+#ifndef FA_BWD_DQ_INTERLEAVE
+#define FA_BWD_DQ_INTERLEAVE 1
+#endif
+// ... of which this many per thread go out at once (fewer values stay live
+// through the dS loop) and the rest spread evenly over its chunks.
+#ifndef FA_BWD_DQ_IMMEDIATE
+#define FA_BWD_DQ_IMMEDIATE 16
+#endif
 #ifndef FA_BWD_COMPUTE_WG_D64
 #define FA_BWD_COMPUTE_WG_D64 2
 #endif
@@ -621,6 +632,11 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     uint32_t ecnt = 0;        // d = 64: units whose dK / dV went out through the dS buffer
     bool epi_pending = false;  // ... the last of which may still be reading it
     int pend_bh = 0, pend_qt = -1;  // dQ partial still to drain from the previous unit
+    constexpr bool kDqInterleave = C::kDqTransposed && FA_BWD_DQ_INTERLEAVE != 0;
+    constexpr int kDqNow = FA_BWD_DQ_IMMEDIATE < kQC ? FA_BWD_DQ_IMMEDIATE : kQC;
+    constexpr int kDqPerChunk = (kQC - kDqNow) / (kQC / 8);  // the dS loop has kQC / 8 chunks
+    static_assert(!kDqInterleave || kDqNow + kDqPerChunk * (kQC / 8) == kQC, "dQ reductions split");
+
     bool ok = true;
     Tracer tr(warp == 0 ? 0 : -1);
 
@@ -750,14 +766,51 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         mbar_arrive(p_full);
         tr(3);
         // ---- dQ partial of the previous query tile ----
+        // d = 128 with FA_BWD_DQ_INTERLEAVE: the drained dQ^T column piece
+        // waiting for its reductions (issued by this tile's dS loop)
+        uint32_t dqv[kDqInterleave ? kQC : 1];
+        float* dq_dst = dq_acc;
+        int dq_nvalid = 0;
+        bool dq_have = false;
         if (DQ && !C::kDqWarpgroup) {
           // dQ of the previous query tile: this unit's, or the last one of
           // the previous unit (deferred so the unit boundary does not wait).
+          int dbh = -1, dqt = 0;  // the partial to drain, if any
           if (x > 0) {
-            if (!(ok = drain_dq(u.bh, u.qtile(x - 1)))) break;
+            dbh = u.bh;
+            dqt = u.qtile(x - 1);
           } else if (pend_qt >= 0) {
-            if (!(ok = drain_dq(pend_bh, pend_qt))) break;
+            dbh = pend_bh;
+            dqt = pend_qt;
             pend_qt = -1;
+          }
+          if (dbh >= 0) {
+            if constexpr (kDqInterleave) {
+              // read this warpgroup's dQ^T columns and release them; the
+              // reductions go out with the dS loop below
+              tr(40);
+              ok = mbar_wait_warp(dq_full, dqcnt & 1, status);
+              ++dqcnt;
+              if (!ok) break;
+              tc_fence_after();
+#pragma unroll
+              for (int c = 0; c < kQC / 32; ++c)
+                tmem_ld32(t_dq + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&dqv[32 * c]));
+              tmem_wait_ld();
+              tc_fence_before();
+              mbar_arrive(dq_empty);
+              tr(41);
+              const int q0 = dqt * kTileRows + kQC * g;
+              dq_dst = dq_acc + ((size_t)dbh * N + q0) * D + r;
+              dq_nvalid = N - q0;
+              dq_have = true;
+              // the first kDqNow now (fewer values live through the dS loop)
+#pragma unroll
+              for (int c = 0; c < kDqNow; ++c)
+                if (c < dq_nvalid) red_add(dq_dst + (size_t)c * D, __uint_as_float(dqv[c]));
+            } else {
+              if (!(ok = drain_dq(dbh, dqt))) break;
+            }
           }
         }
         // ---- dS^T = P^T (dP^T - D) -> shared memory (bf16, swizzled) ----
@@ -812,6 +865,13 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
               if (C::kDsTmem) pk[idx] = dsk[e];  // P^T is no longer needed: keep dS^T for TMEM
             }
             *reinterpret_cast<uint4*>(ds_row + (((cbase + m) ^ swz) * 16)) = make_uint4(dsk[0], dsk[1], dsk[2], dsk[3]);
+            if (kDqInterleave && dq_have) {  // the rest, kDqPerChunk per chunk of eight queries
+#pragma unroll
+              for (int e4 = 0; e4 < kDqPerChunk; ++e4) {
+                const int c = kDqNow + kDqPerChunk * m + e4;
+                if (c < dq_nvalid) red_add(dq_dst + (size_t)c * D, __uint_as_float(dqv[c]));
+              }
+            }
           }
         }
         if (C::kDsTmem) {
@@ -918,7 +978,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
       tr(7);
       if (aborted(abort_flag)) ok = false;
     }
-    if (DQ && ok && pend_qt >= 0) ok = drain_dq(pend_bh, pend_qt);
+    if (DQ && ok && pend_qt >= 0) ok = drain_dq(pend_bh, pend_qt);  // reduced at once: no dS loop follows
     if (!ok) *abort_flag = 1;
     // dK / dV stores still in flight must finish before the CTA exits.
     if (C::kEpiTma && warp == 0 && lane == 0) tma_store_wait_all0();
