@@ -632,7 +632,8 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     uint32_t ecnt = 0;        // d = 64: units whose dK / dV went out through the dS buffer
     bool epi_pending = false;  // ... the last of which may still be reading it
     int pend_bh = 0, pend_qt = -1;  // dQ partial still to drain from the previous unit
-    constexpr bool kDqInterleave = C::kDqTransposed && FA_BWD_DQ_INTERLEAVE != 0;
+    // (not with dropout: its keep bits leave no registers for the held values)
+    constexpr bool kDqInterleave = C::kDqTransposed && FA_BWD_DQ_INTERLEAVE != 0 && !DROP;
     constexpr int kDqNow = FA_BWD_DQ_IMMEDIATE < kQC ? FA_BWD_DQ_IMMEDIATE : kQC;
     constexpr int kDqPerChunk = (kQC - kDqNow) / (kQC / 8);  // the dS loop has kQC / 8 chunks
     static_assert(!kDqInterleave || kDqNow + kDqPerChunk * (kQC / 8) == kQC, "dQ reductions split");
