@@ -19,7 +19,7 @@
 //                      partial is added to the fp32 accumulator.
 //   3. fa_bwd_dq_conv  dQ = scale * accumulator -> bf16.       (HBM-bound)
 //
-// fa_bwd_main roles (n = FA_BWD_COMPUTE_WG compute warpgroups, default 4):
+// fa_bwd_main roles (n compute warpgroups: 2 at d = 64, 4 at d = 128):
 //   warps 0 .. 4n-1   compute warpgroups, thread = key row, warpgroup g owning
 //                     query columns [g 128/n, (g+1) 128/n):
 //                     P^T = 2^(S^T c2 - lse2) -> TMEM (bf16, over the first
@@ -38,11 +38,12 @@
 // dK [256+d, 256+2d); the dQ partial in [384,448) at d = 64, and over dP^T at
 // d = 128 (no columns left).
 // MMA issue order per query tile i:
-//   d = 64:  dV(i) S^T(i+1) | dP^T(i+1) dK(i) dQ(i) | dV(i+1) ...
+//   d = 64:  dV(i) S^T(i+1) | dK(i) dP^T(i+1) dQ(i) | dV(i+1) ...
 //            (dP^T(i+1) as soon as dS(i) is in shared memory; dS is
 //            double-buffered, so dS(i+1) does not wait for dK(i), dQ(i))
 //   d = 128: dP^T(i) | dV(i) S^T(i+1) | dK(i) dQ^T(i) | dP^T(i+1) ...
 //            (dP^T(i+1) waits until dQ^T(i), in its columns, is drained)
+// Q(i) and dO(i) are released right after dK(i), their last reader.
 // so the compute warpgroups' dS(i) overlaps dV(i) and S^T(i+1), and their
 // P(i+1) overlaps the MMAs that follow dS(i).
 #include <cuda.h>
