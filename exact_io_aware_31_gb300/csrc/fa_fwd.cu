@@ -61,9 +61,15 @@ constexpr int kPolyMod = kPolyEvery > 0 ? kPolyEvery : 1;  // divisor that is ne
 static __device__ int g_fa_test_withhold_arrival;
 #endif
 
+// Tuning knob: K/V ring depth at d = 64 (3 to 5 fit in shared memory; 3, 4
+// and 5 measured within 2% of each other).
+#ifndef FA_FWD_STAGES_D64
+#define FA_FWD_STAGES_D64 4
+#endif
+
 template <int D>
 struct FwdCfg {
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kStages = (D == 128) ? 2 : FA_FWD_STAGES_D64;
   static constexpr int kQBufs = (D == 128) ? 1 : 2;  // Q buffers per tile (next unit's Q prefetched at d = 64)
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
@@ -87,6 +93,7 @@ struct FwdCfg {
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct FwdBars {
