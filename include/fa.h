@@ -97,7 +97,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  *   workspace  fa_fwd_splitkv_workspace_size() bytes, 256-byte aligned,
  *             owned by the caller (may be NULL when that size is 0)
  *
- * One launch when a head has one split, else two (splits, then the merge).
+ * One launch when a head has one split, or when a head's splits fit one
+ * thread-block cluster that the device can co-schedule for every head (the
+ * cluster merges in shared memory); else two (splits, then the merge).
  * Errors: FA_ERR_UNSUPPORTED for Nq > 8 or d not in {64, 128};
  * FA_ERR_INVALID_ARG for non-positive sizes, causal with Nq > Nk, a negative
  * num_splits or misaligned pointers; FA_ERR_WORKSPACE for a missing or
@@ -110,8 +112,9 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 /*
  * Workspace bytes fa_fwd_splitkv needs for these sizes (with the current
  * device's SM count when num_splits is 0): the fp32 partial outputs and
- * partial logsumexps of the splits.  0 when one split per head suffices, or
- * when the sizes are invalid (fa_fwd_splitkv then reports the error).
+ * partial logsumexps of the splits.  0 when one split per head suffices or
+ * the splits merge inside a cluster, or when the sizes are invalid
+ * (fa_fwd_splitkv then reports the error).
  */
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
 
