@@ -31,4 +31,5 @@ from .attention import (  # noqa: F401
 )
 from .decode import attention_forward_rect, merge_partials, split_bounds, split_partials  # noqa: F401
 from . import dropout  # noqa: F401
+from . import fp8  # noqa: F401
 from . import io_model  # noqa: F401
