@@ -564,6 +564,100 @@ def run_decode(args, w):
     print(json.dumps(line), flush=True)
 
 
+FP8_METRIC = "attention forward with E4M3 Q, K: TFLOP/s (1 GPU)"
+
+
+def run_fp8(args, w):
+    """Forward with E4M3 queries and keys (fa_fwd_fp8), device-timed, d = 128 workloads.
+
+    Half of the forward's FLOPs (S = Q K^T) run in E4M3, half (P V) in bf16;
+    at the nominal 2:1 ratio of the E4M3 and bf16 dense rates the mix's peak
+    is 4/3 of the measured bf16 peak, the denominator reported here.
+    """
+    import exact_io_aware_31_gb300 as fa
+    from exact_io_aware_31_gb300 import build
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    if w.d != 128:
+        raise SystemExit("--fp8 needs a d = 128 workload")
+    torch.cuda.set_device(local)
+    build.build()
+    fa.load_library()
+    q8, k8, qs, ks, v = workloads.make_fp8_inputs(w.B, w.H, w.N, w.d, w.seed)
+    dev = torch.device("cuda", local)
+    qg, kg, vg = (t.to(dev) for t in (q8, k8, v))
+    o = torch.empty_like(vg)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        st = fa.fa_fwd_fp8(qg.data_ptr(), kg.data_ptr(), vg.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, w.N,
+                           w.d, w.scale, qs, ks, int(w.causal), sh)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd_fp8")
+
+    for _ in range(args.warmup):
+        step()
+        flush_buf.zero_()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in events:
+        flush_buf.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if fa.fa_get_device_status(sh) != fa.FA_OK:
+        raise RuntimeError("device status after the timed region")
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in events)
+    fwd, _ = flops_per_step(w)
+    tflops = fwd / (ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"] * 4.0 / 3.0
+    hq, hk, hv = (t.pin_memory() for t in (q8, k8, v))
+    ho = torch.empty(v.shape, dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for hd, dd in ((hq, qg), (hk, kg), (hv, vg)):
+            dd.copy_(hd, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 10))
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / e2e_steps
+    line = {"metric": FP8_METRIC, "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3 Q K, bf16 V P O, fp32 accumulate", "data": "synthetic",
+            "config": {**w.describe(), "backward": False, "parallelism": "single GPU",
+                       "inputs": "Q, K per-tensor scaled E4M3 codes (descale = max|x| / 448)",
+                       "l2": "flushed before every timed step (2x L2 buffer written)"},
+            "roofline": {"kernel": "fa_fwd_kernel (E4M3 S)", "bound": "tensor", "achieved": round(tflops, 1),
+                         "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "traffic": None, "peak_source": peak_src + " bf16 x 4/3 (half the FLOPs at 2x rate)"},
+            "gpu_launches": args.steps, "clocks": clocks,
+            "e2e": {"value": round(fwd / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv)),
+                    "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "steps": e2e_steps}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -576,6 +670,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=None,
                     help="oracle time per step for --impl reference (default: 150 s spread over all steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true", help="forward with E4M3 Q, K (fa_fwd_fp8) on a d = 128 workload")
     args = ap.parse_args()
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
@@ -589,6 +684,13 @@ def main():
         run_decode(args, workloads.DECODE_BY_NAME[args.workload])
         return
     w = workloads.BY_NAME[args.workload]
+    if args.fp8:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the bf16 "
+                              "forward/backward workloads"}))
+            return
+        run_fp8(args, w)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:

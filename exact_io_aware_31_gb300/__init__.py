@@ -6,12 +6,12 @@ device memory and streams.  There is no fallback: if the library is missing
 or the device is not sm_103, calls raise.
 
 Raw entry points (same names and argument order as the C ABI, pointers as
-ints):  ``fa_fwd``, ``fa_bwd``, ``fa_bwd_workspace_size``, the three phases
+ints):  ``fa_fwd``, ``fa_fwd_fp8``, ``fa_bwd``, ``fa_bwd_workspace_size``, the three phases
 of ``fa_bwd`` (``fa_bwd_preprocess``, ``fa_bwd_dkdv``, ``fa_bwd_dq_convert``),
 the split-KV decode forward (``fa_fwd_splitkv``,
 ``fa_fwd_splitkv_workspace_size``), ``fa_get_device_status``,
 ``fa_status_string``.
-Tensor helpers: :func:`forward`, :func:`backward`, :func:`decode_forward`.
+Tensor helpers: :func:`forward`, :func:`forward_fp8`, :func:`backward`, :func:`decode_forward`.
 """
 
 from __future__ import annotations
@@ -20,7 +20,7 @@ import ctypes
 import os
 
 __all__ = [
-    "LIB_PATH", "FaError", "load_library", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_deterministic",
+    "LIB_PATH", "FaError", "load_library", "fa_fwd", "fa_fwd_fp8", "forward_fp8", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_deterministic",
     "fa_fwd_dropout", "fa_bwd_dropout",
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "decode_forward",
@@ -39,7 +39,7 @@ FA_ERR_CUDA = 4
 FA_ERR_DEVICE_TIMEOUT = 5
 FA_ERR_INTERNAL = 6
 
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_deterministic", "fa_fwd_dropout",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_deterministic", "fa_fwd_dropout",
                     "fa_bwd_dropout", "fa_bwd_preprocess",
                     "fa_bwd_dkdv",
                     "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.fa_fwd.restype = i
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, f, i, vp]
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd.restype = i
@@ -104,6 +106,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 # ------------------------------------------------------------- raw C ABI ----
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+
+
+def fa_fwd_fp8(q8, k8, v, o, lse, B, H, N, d, scale, q_descale, k_descale, causal, stream) -> int:
+    return load_library().fa_fwd_fp8(q8, k8, v, o, lse, B, H, N, d, scale, q_descale, k_descale, causal, stream)
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:
@@ -200,6 +206,29 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
                 float(scale), int(bool(causal)), _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
+    return o, l
+
+
+def forward_fp8(q8, k8, v, q_descale=1.0, k_descale=1.0, scale=None, causal=False, out=None, lse=None,
+                stream=None):
+    """Forward with E4M3 queries and keys (``torch.float8_e4m3fn`` or their ``uint8`` codes,
+    [B, H, N, 128]) and bf16 values; returns ``(o, lse)``."""
+    import torch
+    B, H, N, d = q8.shape
+    for name, t in (("q8", q8), ("k8", k8)):
+        want = t.dtype if t.dtype in (torch.uint8, torch.float8_e4m3fn) else torch.float8_e4m3fn
+        _check(t, name, (B, H, N, d), want)
+    _check(v, "v", (B, H, N, d), torch.bfloat16)
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty_like(v) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=v.device) if lse is None else lse
+    _check(o, "out", (B, H, N, d), torch.bfloat16)
+    _check(l, "lse", (B, H, N), torch.float32)
+    st = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, N, d,
+                    float(scale), float(q_descale), float(k_descale), int(bool(causal)), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_fp8")
     return o, l
 
 

@@ -105,6 +105,19 @@ int make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// [B*H, N, d] E4M3 codes (one byte each) for the FP8 forward, d = 128: one
+// 128-row x 128-column box is one 128-byte-swizzled block.
+int make_map_e4m3(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)N * d};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_sizes(int B, int H, int N, int d, float scale, int causal) {
@@ -171,6 +184,45 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   a.d = d;
   a.causal = causal;
   a.c2 = log2_scale(scale);
+  a.status = dev->status;
+  const int units = fwd_units(BH, N);
+  a.grid = units < dev->sms ? units : dev->sms;
+  if (launch_fwd(a, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o, float* lse, int B, int H, int N,
+                          int d, float scale, float q_descale, float k_descale, int causal, cudaStream_t stream) {
+  int st = check_sizes(B, H, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(q_descale) || !std::isfinite(k_descale) || q_descale < 0.f || k_descale < 0.f)
+    return FA_ERR_INVALID_ARG;
+  const float eff = scale * q_descale * k_descale;
+  if (!std::isfinite(eff)) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (make_map_e4m3(&tq, q8, BH, N, d) || make_map_e4m3(&tk, k8, BH, N, d) || make_map(&tv, v, BH, N, d))
+    return FA_ERR_CUDA;
+  FwdLaunch a;
+  a.tm_q = &tq;
+  a.tm_k = &tk;
+  a.tm_v = &tv;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.c2 = log2_scale(eff);
+  a.fp8 = 1;
   a.status = dev->status;
   const int units = fwd_units(BH, N);
   a.grid = units < dev->sms ? units : dev->sms;

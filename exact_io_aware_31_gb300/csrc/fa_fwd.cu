@@ -67,12 +67,16 @@ static __device__ int g_fa_test_withhold_arrival;
 #define FA_FWD_STAGES_D64 4
 #endif
 
-template <int D>
+template <int D, bool F8 = false>
 struct FwdCfg {
   static constexpr int kStages = (D == 128) ? 2 : FA_FWD_STAGES_D64;
   static constexpr int kQBufs = (D == 128) ? 1 : 2;  // Q buffers per tile (next unit's Q prefetched at d = 64)
-  static constexpr int kTileBytes = kTileRows * D * 2;
-  static constexpr int kBlocks = D / 64;
+  static constexpr int kTileBytes = kTileRows * D * 2;  // a bf16 tile (V; Q and K unless F8)
+  static constexpr int kBlocks = D / 64;                // its 128-byte-swizzled 64-column blocks
+  // F8: Q and K tiles hold E4M3 codes, one byte an element: 128-column blocks
+  static constexpr int kQKBytes = F8 ? kTileRows * D : kTileBytes;
+  static constexpr int kQKBlocks = F8 ? D / 128 : kBlocks;
+  static constexpr int kQKBlockCols = F8 ? 128 : 64;
   static constexpr int kTmemCols = 512;
   // d = 64: P_t has TMEM columns of its own, so S_t(j+1) is issued as soon as
   // the softmax has read S_t(j) and runs while P_t(j) is being computed.  At
@@ -86,8 +90,8 @@ struct FwdCfg {
   static constexpr int threads(bool pvw) { return pvw ? 352 : 320; }
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kQBufs * kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffK = kOffQ + 2 * kQBufs * kQKBytes;
+  static constexpr int kOffV = kOffK + kStages * kQKBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   static constexpr int kNumBars = 2 * 2 * kQBufs + 4 * kStages + 5 * 2 + 1;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
@@ -149,13 +153,14 @@ __device__ __forceinline__ FwdUnit fwd_decode(int pos, int BH, int nqb, int N, i
 // DROP: dropout on the probabilities (fa_dropout.cuh): the row sum l keeps
 // every probability, the P fed to P V keeps only the surviving ones, and the
 // epilogue scales O by 1 / (1 - p).
-template <int D, bool CAUSAL, bool DROP, bool PVW>
-__global__ void __launch_bounds__(FwdCfg<D>::threads(PVW), 1)
+template <int D, bool CAUSAL, bool DROP, bool PVW, bool F8 = false>
+__global__ void __launch_bounds__(FwdCfg<D, F8>::threads(PVW), 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ lse, int BH, int N, float c2, DropParams dp, int* status) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
   static_assert(!PVW || C::kSepP, "the P V warp needs P in columns of its own");
+  static_assert(!F8 || (D == 128 && !DROP && !PVW), "FP8 Q, K: d = 128, no dropout, one issuer");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
   uint8_t* sm = smem_raw;
@@ -239,10 +244,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::threads(PVW), 1)
           ok = mbar_wait(&B.q_empty[qb], ((qcnt[t] / C::kQBufs) & 1) ^ 1, status);
           tr(31);
           if (!ok) break;
-          uint8_t* dst = sm + C::kOffQ + qb * C::kTileBytes;
-          mbar_expect_tx(&B.q_full[qb], C::kTileBytes);
-          for (int kb = 0; kb < C::kBlocks; ++kb)
-            tma_load_3d(dst + kb * kSwzBlockBytes, &tm_q, &B.q_full[qb], kb * 64, u.q0 + t * kTileRows, u.bh);
+          uint8_t* dst = sm + C::kOffQ + qb * C::kQKBytes;
+          mbar_expect_tx(&B.q_full[qb], C::kQKBytes);
+          for (int kb = 0; kb < C::kQKBlocks; ++kb)
+            tma_load_3d(dst + kb * kSwzBlockBytes, &tm_q, &B.q_full[qb], kb * C::kQKBlockCols, u.q0 + t * kTileRows,
+                        u.bh);
           ++qcnt[t];
         }
         for (int j = 0; j < u.nkv_max && ok; ++j, ++kv_it) {
@@ -252,11 +258,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::threads(PVW), 1)
           ok = mbar_wait(&B.kv_empty[st], ph ^ 1, status);
           tr(33);
           if (!ok) break;
-          uint8_t* kd = sm + C::kOffK + st * C::kTileBytes;
+          uint8_t* kd = sm + C::kOffK + st * C::kQKBytes;
           uint8_t* vd = sm + C::kOffV + st * C::kTileBytes;
-          mbar_expect_tx(&B.k_full[st], C::kTileBytes);
-          for (int kb = 0; kb < C::kBlocks; ++kb)
-            tma_load_3d(kd + kb * kSwzBlockBytes, &tm_k, &B.k_full[st], kb * 64, j * kTileRows, u.bh);
+          mbar_expect_tx(&B.k_full[st], C::kQKBytes);
+          for (int kb = 0; kb < C::kQKBlocks; ++kb)
+            tma_load_3d(kd + kb * kSwzBlockBytes, &tm_k, &B.k_full[st], kb * C::kQKBlockCols, j * kTileRows, u.bh);
           if (PVW && !(ok = mbar_wait(&B.v_empty[st], ph ^ 1, status))) break;
           mbar_expect_tx(&B.v_full[st], C::kTileBytes);
           for (int kb = 0; kb < C::kBlocks; ++kb)
@@ -312,12 +318,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::threads(PVW), 1)
             tc_fence_after();
           }
           ++sis[t];
-          const uint32_t qa = q_s + qbuf[t] * C::kTileBytes, ka = k_s + st * C::kTileBytes;
+          const uint32_t qa = q_s + qbuf[t] * C::kQKBytes, ka = k_s + st * C::kQKBytes;
+          // 32 bytes of the 128-byte swizzled rows a step: 16 bf16 or 32 E4M3 elements
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
+          for (int k = 0; k < D / (F8 ? 32 : 16); ++k) {
             const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
-            mma_ss_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdescS,
-                   k > 0);
+            if constexpr (F8)
+              mma_ss_f8_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024),
+                          idesc_e4m3(128, 128), k > 0);
+            else
+              mma_ss_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdescS,
+                       k > 0);
           }
           mma_commit_w(&B.s_full[t]);
           return true;
@@ -707,10 +718,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::threads(PVW), 1)
   }
 }
 
-template <int D, bool CAUSAL, bool DROP, bool PVW = false>
+template <int D, bool CAUSAL, bool DROP, bool PVW = false, bool F8 = false>
 static cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
-  using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, DROP, PVW>;
+  using C = FwdCfg<D, F8>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, DROP, PVW, F8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<a.grid, C::threads(PVW), C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v,
@@ -733,6 +744,9 @@ static cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.fp8)  // E4M3 Q and K, d = 128 (checked by the caller)
+    return a.causal ? launch_fwd_t<128, true, false, false, true>(a, stream)
+                    : launch_fwd_t<128, false, false, false, true>(a, stream);
   if (a.dropout) return a.d == 64 ? launch_fwd_d<64, true>(a, stream) : launch_fwd_d<128, true>(a, stream);
   return a.d == 64 ? launch_fwd_d<64, false>(a, stream) : launch_fwd_d<128, false>(a, stream);
 }

@@ -22,6 +22,7 @@ struct FwdLaunch {
   int grid;
   int dropout = 0;  // 1: dropout on the probabilities with `drop`
   DropParams drop;
+  int fp8 = 0;      // 1: tm_q, tm_k are E4M3 codes (d = 128); c2 includes their descale factors
 };
 
 struct BwdLaunch {

@@ -285,6 +285,17 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint6
       : "memory");
 }
 
+// kind::f8f6f4 with A and B in shared memory (K = 32 one-byte elements an
+// instruction); the instruction descriptor selects the 8-bit formats.
+__device__ __forceinline__ void mma_ss_f8_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 t;\n\telect.sync t|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t.reg .b32 t;\n\telect.sync t|e, 0xffffffff;\n\t"
@@ -362,6 +373,14 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, ui
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, shape
 // M x N; a_mn / b_mn select MN-major (transposed) operands.
+// Instruction descriptor, kind::f8f6f4: E4M3 A and B (format code 0 in both
+// type fields), fp32 accumulator, shape M x N, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                  // D format: f32
+         | (0u << 7) | (0u << 10)   // A, B format: E4M3
+         | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4)                  // D format: f32
          | (1u << 7)                // A format: bf16

@@ -79,6 +79,29 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            float scale, int causal, cudaStream_t stream);
 
 /*
+ * Forward with FP8 queries and keys.  [L] "Key ideas": FlashAttention-3 adds
+ * FP8.  Q and K arrive as E4M3 codes (OCP FP8: 1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN, largest 448),
+ * each tensor with one descale factor: the real value of an element is its
+ * decoded code times the factor.  S = Q K^T runs on the tensor cores in E4M3
+ * with fp32 accumulation (every product of two E4M3 values is exact in
+ * fp32); P and V stay bf16.
+ *
+ *   q8, k8    in   [B, H, N, d] E4M3 codes, one byte each, d = 128
+ *   v         in   [B, H, N, d] bf16
+ *   o, lse    out  as fa_fwd, for the scores scale * q_descale * k_descale *
+ *                  (decoded Q)(decoded K)^T
+ *   q_descale, k_descale  finite, >= 0
+ *
+ * One persistent kernel launch.  A NaN code makes the rows it reaches NaN.
+ * Errors as fa_fwd, plus FA_ERR_UNSUPPORTED for d != 128 and
+ * FA_ERR_INVALID_ARG for a negative or non-finite descale (or a non-finite
+ * product with scale).
+ */
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o, float* lse, int B, int H, int N, int d,
+               float scale, float q_descale, float k_descale, int causal, cudaStream_t stream);
+
+/*
  * Split-KV forward for decoding.  [L] FAQ "Does FlashAttention help during
  * LLM decoding?": a decode step has one query (or a few) per sequence, the
  * cost is reading the key/value cache, and Flash-Decoding spreads that read

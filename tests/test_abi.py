@@ -26,7 +26,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_names():
@@ -35,7 +35,7 @@ def test_header_declares_the_binding_names():
 
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH], capture_output=True, text=True).stdout
-    exported = set(re.findall(r"\sT\s(fa_[a-z_]+)$", out, flags=re.M))
+    exported = set(re.findall(r"\sT\s(fa_[a-z0-9_]+)$", out, flags=re.M))
     for name in declared_functions():
         assert name in exported, name
         assert hasattr(lib, name)
@@ -162,3 +162,30 @@ def test_dropout_rate_validation(lib, p):
     assert fa.fa_fwd_dropout(A, A, A, A, A, 1, 1, 16, 64, 0.125, 0, p, 1, 0, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_bwd_dropout(A, A, A, A, A, A, A, A, A, 1, 1, 16, 64, 0.125, 0, p, 1, 0, A, 1 << 30,
                              None) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(q_descale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(k_descale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(k_descale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(q_descale=3e38, k_descale=3e38), fa.FA_ERR_INVALID_ARG),   # product with scale overflows
+    (dict(q8=A + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(v=None), fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_fp8_validation(lib, kw, code):
+    args = dict(q8=A, k8=A, v=A, o=A, lse=A, B=1, H=1, N=16, d=128, scale=0.125, q_descale=1.0, k_descale=1.0,
+                causal=0, stream=None)
+    args.update(kw)
+    assert fa.fa_fwd_fp8(**args) == code
+
+
+def test_fp8_helper_rejects_cpu_tensors(lib):
+    import torch
+    q8 = torch.zeros(1, 1, 8, 128, dtype=torch.uint8)
+    v = torch.zeros(1, 1, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.forward_fp8(q8, q8, v)

@@ -98,6 +98,25 @@ def make_inputs(B, H, N, d, seed, stress=None):
     return tuple(t.to(torch.bfloat16) for t in (q, k, v, do))
 
 
+def make_fp8_inputs(B, H, N, d, seed, stress=None):
+    """Seeded E4M3 codes for Q and K, their descale factors, and bf16 V, on the CPU.
+
+    Q, K, V are drawn as in :func:`make_inputs` (same seed, same stress); Q and K
+    are then stored per tensor as E4M3 codes: descale = max|x| / 448 (so the
+    largest element lands on the largest finite code) and code = the
+    round-to-nearest E4M3 of x / descale (PyTorch's float8_e4m3fn conversion),
+    returned as uint8.  Both the CUDA path and the oracle consume these codes.
+    """
+    q, k, v, _ = make_inputs(B, H, N, d, seed, stress)
+    out = []
+    for t in (q, k):
+        x = t.float()
+        descale = max(float(x.abs().max()), 1e-30) / 448.0
+        out.append(((x / descale).to(torch.float8_e4m3fn).view(torch.uint8), descale))
+    (q8, q_descale), (k8, k_descale) = out
+    return q8, k8, q_descale, k_descale, v
+
+
 def replica_seed(w: Workload, rank: int = 0) -> int:
     """Seed of rank ``rank``'s batch: rank 0 draws the workload's own inputs,
     every other rank an independent batch of the same shape."""
