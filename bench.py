@@ -88,6 +88,7 @@ def load_peaks():
 # headers it includes (host-side launch plumbing is not part of it).
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cu"],
+    "fa_fwd_kernel_fp8": ["fa_fwd.cu"],
     "fa_bwd_pre": ["fa_bwd.cu"],
     "fa_bwd_main": ["fa_bwd.cu"],
     "fa_bwd_dq_conv": ["fa_bwd.cu"],
@@ -650,7 +651,8 @@ def run_fp8(args, w):
                        "l2": "flushed before every timed step (2x L2 buffer written)"},
             "roofline": {"kernel": "fa_fwd_kernel (E4M3 S)", "bound": "tensor", "achieved": round(tflops, 1),
                          "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                         "traffic": None, "peak_source": peak_src + " bf16 x 4/3 (half the FLOPs at 2x rate)"},
+                         "traffic": dram_traffic("fa_fwd_kernel_fp8", w.name),
+                         "peak_source": peak_src + " bf16 x 4/3 (half the FLOPs at 2x rate)"},
             "gpu_launches": args.steps, "clocks": clocks,
             "e2e": {"value": round(fwd / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv)),
