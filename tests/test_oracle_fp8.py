@@ -83,3 +83,23 @@ def test_representable_inputs_equal_the_plain_oracle():
     k = torch.from_numpy(k8).view(torch.float8_e4m3fn).to(torch.float64).numpy() * 2.0
     o_ref, lse_ref = oracle.attention_forward(q, k, v, 0.2, True)
     assert np.allclose(o, o_ref, rtol=0, atol=1e-12) and np.allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_fp8_input_generator_codes():
+    """The seeded E4M3 inputs the GPU tests and the bench share: no NaN codes,
+    the largest |x| lands on code 448, and every decoded value is x rounded to
+    E4M3 (relative error <= 2^-4 in the normal range, absolute <= 2^-10 times
+    the descale below it)."""
+    import workloads
+    q8, k8, qs, ks, v = workloads.make_fp8_inputs(1, 2, 300, 128, seed=11, stress="wide")
+    q, k, _, _ = workloads.make_inputs(1, 2, 300, 128, seed=11, stress="wide")
+    assert v.dtype == torch.bfloat16 and q8.dtype == torch.uint8 and k8.dtype == torch.uint8
+    for codes, x, ds in ((q8, q, qs), (k8, k, ks)):
+        c = codes.numpy()
+        assert not np.any((c & 0x7F) == 0x7F)
+        dec = fp8.e4m3_decode(c)
+        xs = x.double().numpy() / ds
+        assert np.abs(dec).max() == 448.0
+        normal = np.abs(xs) >= 2.0 ** -6
+        assert np.all(np.abs(dec[normal] - xs[normal]) <= 2.0 ** -4 * np.abs(xs[normal]))
+        assert np.all(np.abs(dec[~normal] - xs[~normal]) <= 2.0 ** -10)
