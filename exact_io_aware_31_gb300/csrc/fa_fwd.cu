@@ -33,6 +33,11 @@
 // one issuer cannot keep up with the softmax warpgroups that share its
 // sub-partition.  Measured faster for units of 8 or more key tiles and slower
 // for the short causal units of N <= 1024, so the launch picks it by shape.
+// F8 (d = 128): Q and K arrive as E4M3 codes (lensaml.com "FlashAttention",
+// "Key ideas", FlashAttention-3's FP8); each tile is one 128-byte-swizzled
+// block of 128 one-byte columns, S = Q K^T issues kind::f8f6f4 MMAs (K = 32
+// a step), and everything after S is the bf16 path, the two descale factors
+// folded into c2 by the host.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

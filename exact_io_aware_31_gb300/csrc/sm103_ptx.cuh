@@ -373,20 +373,20 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, ui
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, shape
 // M x N; a_mn / b_mn select MN-major (transposed) operands.
-// Instruction descriptor, kind::f8f6f4: E4M3 A and B (format code 0 in both
-// type fields), fp32 accumulator, shape M x N, both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
-  return (1u << 4)                  // D format: f32
-         | (0u << 7) | (0u << 10)   // A, B format: E4M3
-         | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4)                  // D format: f32
          | (1u << 7)                // A format: bf16
          | (1u << 10)               // B format: bf16
          | ((uint32_t)a_mn << 15)   // A major-ness
          | ((uint32_t)b_mn << 16)   // B major-ness
+         | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4: E4M3 A and B (format code 0 in both
+// type fields), fp32 accumulator, shape M x N, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                  // D format: f32
+         | (0u << 7) | (0u << 10)   // A, B format: E4M3
          | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
