@@ -158,6 +158,36 @@ WorkspaceLayout workspace_layout(int B, int H, int N, int d) {
   return w;
 }
 
+// The forward's launch once the arguments are validated and the tensor maps
+// built (shared by fa_fwd, fa_fwd_fp8 and fa_fwd_dropout).  c2 = scale (times
+// the FP8 descale factors) * log2(e); `drop` is used when dropout != 0.
+int run_forward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o, float* lse, int BH,
+                int N, int d, int causal, float c2, const DeviceInfo& dev, int fp8, int dropout, const DropParams& drop,
+                cudaStream_t stream) {
+  FwdLaunch a;
+  a.tm_q = &tq;
+  a.tm_k = &tk;
+  a.tm_v = &tv;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.c2 = c2;
+  a.status = dev.status;
+  a.fp8 = fp8;
+  a.dropout = dropout;
+  a.drop = drop;
+  const int units = fwd_units(BH, N);
+  a.grid = units < dev.sms ? units : dev.sms;
+  if (launch_fwd(a, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -173,25 +203,7 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   const int BH = B * H;
   CUtensorMap tq, tk, tv;
   if (make_map(&tq, q, BH, N, d) || make_map(&tk, k, BH, N, d) || make_map(&tv, v, BH, N, d)) return FA_ERR_CUDA;
-  FwdLaunch a;
-  a.tm_q = &tq;
-  a.tm_k = &tk;
-  a.tm_v = &tv;
-  a.o = o;
-  a.lse = lse;
-  a.BH = BH;
-  a.N = N;
-  a.d = d;
-  a.causal = causal;
-  a.c2 = log2_scale(scale);
-  a.status = dev->status;
-  const int units = fwd_units(BH, N);
-  a.grid = units < dev->sms ? units : dev->sms;
-  if (launch_fwd(a, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return FA_ERR_CUDA;
-  }
-  return FA_OK;
+  return run_forward(tq, tk, tv, o, lse, BH, N, d, causal, log2_scale(scale), *dev, 0, 0, DropParams{}, stream);
 }
 
 extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o, float* lse, int B, int H, int N,
@@ -211,26 +223,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o
   CUtensorMap tq, tk, tv;
   if (make_map_e4m3(&tq, q8, BH, N, d) || make_map_e4m3(&tk, k8, BH, N, d) || make_map(&tv, v, BH, N, d))
     return FA_ERR_CUDA;
-  FwdLaunch a;
-  a.tm_q = &tq;
-  a.tm_k = &tk;
-  a.tm_v = &tv;
-  a.o = o;
-  a.lse = lse;
-  a.BH = BH;
-  a.N = N;
-  a.d = d;
-  a.causal = causal;
-  a.c2 = log2_scale(eff);
-  a.fp8 = 1;
-  a.status = dev->status;
-  const int units = fwd_units(BH, N);
-  a.grid = units < dev->sms ? units : dev->sms;
-  if (launch_fwd(a, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return FA_ERR_CUDA;
-  }
-  return FA_OK;
+  return run_forward(tq, tk, tv, o, lse, BH, N, d, causal, log2_scale(eff), *dev, 1, 0, DropParams{}, stream);
 }
 
 namespace fa {
@@ -393,27 +386,7 @@ extern "C" int fa_fwd_dropout(const void* q, const void* k, const void* v, void*
   const int BH = B * H;
   CUtensorMap tq, tk, tv;
   if (make_map(&tq, q, BH, N, d) || make_map(&tk, k, BH, N, d) || make_map(&tv, v, BH, N, d)) return FA_ERR_CUDA;
-  FwdLaunch a;
-  a.tm_q = &tq;
-  a.tm_k = &tk;
-  a.tm_v = &tv;
-  a.o = o;
-  a.lse = lse;
-  a.BH = BH;
-  a.N = N;
-  a.d = d;
-  a.causal = causal;
-  a.c2 = log2_scale(scale);
-  a.status = dev->status;
-  a.dropout = 1;
-  a.drop = dp;
-  const int units = fwd_units(BH, N);
-  a.grid = units < dev->sms ? units : dev->sms;
-  if (launch_fwd(a, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return FA_ERR_CUDA;
-  }
-  return FA_OK;
+  return run_forward(tq, tk, tv, o, lse, BH, N, d, causal, log2_scale(scale), *dev, 0, 1, dp, stream);
 }
 
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
