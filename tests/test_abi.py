@@ -189,3 +189,44 @@ def test_fp8_helper_rejects_cpu_tensors(lib):
     v = torch.zeros(1, 1, 8, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.forward_fp8(q8, q8, v)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(o=A + 4), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(workspace=None), fa.FA_ERR_WORKSPACE),
+    (dict(workspace_bytes=1024), fa.FA_ERR_WORKSPACE),
+])
+def test_bwd_preprocess_validation(lib, kw, code):
+    args = dict(o=A, dout=A, lse=A, B=1, H=1, N=16, d=64, workspace=A, workspace_bytes=1 << 30, stream=None)
+    args.update(kw)
+    assert fa.fa_bwd_preprocess(**args) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(causal=5), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(dv=A + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(dout=None), fa.FA_ERR_INVALID_ARG),
+    (dict(workspace=A + 128), fa.FA_ERR_WORKSPACE),
+])
+def test_bwd_dkdv_validation(lib, kw, code):
+    args = dict(q=A, k=A, v=A, dout=A, dk=A, dv=A, B=1, H=1, N=16, d=64, scale=0.125, causal=1, workspace=A,
+                workspace_bytes=1 << 30, stream=None)
+    args.update(kw)
+    assert fa.fa_bwd_dkdv(**args) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dq=A + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(workspace=None), fa.FA_ERR_WORKSPACE),
+])
+def test_bwd_dq_convert_validation(lib, kw, code):
+    args = dict(dq=A, B=1, H=1, N=16, d=64, scale=0.125, workspace=A, workspace_bytes=1 << 30, stream=None)
+    args.update(kw)
+    assert fa.fa_bwd_dq_convert(**args) == code
