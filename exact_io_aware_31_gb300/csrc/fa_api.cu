@@ -11,6 +11,7 @@
 
 #include "../../include/fa.h"
 #include "fa_common.cuh"
+#include "fa_context.h"
 #include "fa_kernels.h"
 
 namespace fa {
@@ -23,59 +24,68 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Facts about the current device plus the status word's address in the
+// current context.
 struct DeviceInfo {
+  int sms = 0;
+  bool sm103 = false;
+  int* status = nullptr;  // device address of g_device_status in the current context
+};
+
+struct DeviceProps {
   bool ready = false;
   int sms = 0;
   bool sm103 = false;
-  int* status = nullptr;  // device address of g_device_status
 };
 
 std::mutex g_mu;
-DeviceInfo g_dev[kMaxDevices];
+DeviceProps g_dev[kMaxDevices];
+PerContextAddress g_status_addr;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// Resolve per-device facts once, with that device current.
-int device_info(DeviceInfo** out) {
+// Device properties are resolved once per device; the status word's address
+// once per context (a device address is only valid in the context that gave
+// it).
+int device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return FA_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lock(g_mu);
-  DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
-    int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      cudaGetLastError();
-      return FA_ERR_CUDA;
-    }
-    d.sm103 = (major == 10 && minor == 3);
-    d.sms = sms;
-    if (d.sm103) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceProps& d = g_dev[dev];
+    if (!d.ready) {
+      int major = 0, minor = 0, sms = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         cudaGetLastError();
         return FA_ERR_CUDA;
       }
-      d.status = static_cast<int*>(p);
-    }
-    if (!g_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-              cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || fn == nullptr) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
+      if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+          cudaGetLastError();
+          return FA_ERR_CUDA;
+        }
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
       }
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      d.sm103 = (major == 10 && minor == 3);
+      d.sms = sms;
+      d.ready = true;
     }
-    d.ready = true;
+    out->sms = d.sms;
+    out->sm103 = d.sm103;
   }
-  if (!d.sm103) return FA_ERR_UNSUPPORTED;
-  *out = &d;
+  if (!out->sm103) return FA_ERR_UNSUPPORTED;
+  void* p = nullptr;
+  if (g_status_addr.get(&p, [](void** q) { return cudaGetSymbolAddress(q, g_device_status); }) != 0)
+    return FA_ERR_CUDA;
+  out->status = static_cast<int*>(p);
   return FA_OK;
 }
 
@@ -198,12 +208,12 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   int st = check_sizes(B, H, N, d, scale, causal);
   if (st != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
-  DeviceInfo* dev = nullptr;
+  DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap tq, tk, tv;
   if (make_map(&tq, q, BH, N, d) || make_map(&tk, k, BH, N, d) || make_map(&tv, v, BH, N, d)) return FA_ERR_CUDA;
-  return run_forward(tq, tk, tv, o, lse, BH, N, d, causal, log2_scale(scale), *dev, 0, 0, DropParams{}, stream);
+  return run_forward(tq, tk, tv, o, lse, BH, N, d, causal, log2_scale(scale), dev, 0, 0, DropParams{}, stream);
 }
 
 extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o, float* lse, int B, int H, int N,
@@ -217,13 +227,13 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o
   if (d != 128) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
-  DeviceInfo* dev = nullptr;
+  DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap tq, tk, tv;
   if (make_map_e4m3(&tq, q8, BH, N, d) || make_map_e4m3(&tk, k8, BH, N, d) || make_map(&tv, v, BH, N, d))
     return FA_ERR_CUDA;
-  return run_forward(tq, tk, tv, o, lse, BH, N, d, causal, log2_scale(eff), *dev, 1, 0, DropParams{}, stream);
+  return run_forward(tq, tk, tv, o, lse, BH, N, d, causal, log2_scale(eff), dev, 1, 0, DropParams{}, stream);
 }
 
 namespace fa {
@@ -306,11 +316,11 @@ int current_device() {
 
 extern "C" size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (check_decode(B, H, Nq, Nk, d, 1.0f, 0, num_splits) != FA_OK) return 0;
-  DeviceInfo* dev = nullptr;
+  DeviceInfo dev;
   if (device_info(&dev) != FA_OK) return 0;
   const long long bh = (long long)B * H;
   bool cluster = false;
-  const int splits = decode_plan(current_device(), bh, Nq, Nk, d, num_splits, dev->sms, &cluster);
+  const int splits = decode_plan(current_device(), bh, Nq, Nk, d, num_splits, dev.sms, &cluster);
   return decode_partials_bytes(bh, Nq, d, splits, cluster);
 }
 
@@ -320,12 +330,12 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   int st = check_decode(B, H, Nq, Nk, d, scale, causal, num_splits);
   if (st != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
-  DeviceInfo* dev = nullptr;
+  DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
   const int BH = B * H;
   DecLaunch a;
   bool cluster = false;
-  a.splits = decode_plan(current_device(), BH, Nq, Nk, d, num_splits, dev->sms, &cluster);
+  a.splits = decode_plan(current_device(), BH, Nq, Nk, d, num_splits, dev.sms, &cluster);
   a.cluster = cluster ? 1 : 0;
   const size_t need = decode_partials_bytes(BH, Nq, d, a.splits, cluster);
   if (need > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
@@ -347,7 +357,7 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   a.d = d;
   a.causal = causal;
   a.c2 = log2_scale(scale);
-  a.status = dev->status;
+  a.status = dev.status;
   if (launch_decode(a, stream) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
@@ -381,12 +391,12 @@ extern "C" int fa_fwd_dropout(const void* q, const void* k, const void* v, void*
   if (st != FA_OK) return st;
   if ((st = check_sizes(B, H, N, d, scale, causal)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
-  DeviceInfo* dev = nullptr;
+  DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap tq, tk, tv;
   if (make_map(&tq, q, BH, N, d) || make_map(&tk, k, BH, N, d) || make_map(&tv, v, BH, N, d)) return FA_ERR_CUDA;
-  return run_forward(tq, tk, tv, o, lse, BH, N, d, causal, log2_scale(scale), *dev, 0, 1, dp, stream);
+  return run_forward(tq, tk, tv, o, lse, BH, N, d, causal, log2_scale(scale), dev, 0, 1, dp, stream);
 }
 
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -414,7 +424,7 @@ int prepare_bwd(BwdLaunch& a, CUtensorMap* maps, unsigned need, const void* q, c
   const WorkspaceLayout w = workspace_layout(B, H, N, d);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
     return FA_ERR_WORKSPACE;
-  DeviceInfo* dev = nullptr;
+  DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
   const int BH = B * H;
   if (need & kNeedQKV) {
@@ -449,10 +459,10 @@ int prepare_bwd(BwdLaunch& a, CUtensorMap* maps, unsigned need, const void* q, c
   a.causal = causal;
   a.scale = scale;
   a.c2 = log2_scale(scale);
-  a.status = dev->status;
+  a.status = dev.status;
   const int units = bwd_units(BH, N);
-  a.grid = units < dev->sms ? units : dev->sms;
-  a.pre_grid = dev->sms * 8;
+  a.grid = units < dev.sms ? units : dev.sms;
+  a.pre_grid = dev.sms * 8;
   return FA_OK;
 }
 
@@ -507,10 +517,10 @@ extern "C" int fa_bwd_deterministic(const void* q, const void* k, const void* v,
                        lse, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes);
   if (st != FA_OK) return st;
   a.with_dq = 0;  // dK / dV kernel without dQ; dQ from the query-outer kernel
-  DeviceInfo* dev = nullptr;
+  DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
   const int units = bwd_dq_units(a.BH, N);
-  a.dq_grid = units < dev->sms ? units : dev->sms;
+  a.dq_grid = units < dev.sms ? units : dev.sms;
   if ((st = cuda_status(launch_bwd_pre(a, stream))) != FA_OK) return st;
   if ((st = cuda_status(launch_bwd_main(a, stream))) != FA_OK) return st;
   return cuda_status(launch_bwd_dq(a, stream));
@@ -548,7 +558,7 @@ extern "C" int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float sca
 }
 
 extern "C" int fa_get_device_status(cudaStream_t stream) {
-  DeviceInfo* dev = nullptr;
+  DeviceInfo dev;
   int st = device_info(&dev);
   if (st != FA_OK) return st;
   if (cudaStreamSynchronize(stream) != cudaSuccess) {
@@ -556,8 +566,8 @@ extern "C" int fa_get_device_status(cudaStream_t stream) {
     return FA_ERR_CUDA;
   }
   int value = 0, zero = 0;
-  if (cudaMemcpy(&value, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+  if (cudaMemcpy(&value, dev.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(dev.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
   }

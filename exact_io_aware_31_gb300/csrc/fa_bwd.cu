@@ -57,46 +57,17 @@
 
 namespace fa {
 
-// Tuning knob: at d = 128, drain the dQ partial with a dedicated warpgroup (1)
-// or from the compute warpgroups (0).  Measured on GB300 the dedicated
-// warpgroup was slower (its 128-register rows cap the whole CTA at 128
-// registers and it still serialises the next dP^T behind its reductions).
-#ifndef FA_BWD_DQ_WARPGROUP
-#define FA_BWD_DQ_WARPGROUP 0
-#endif
-
-// Tuning knob: in the backward's P^T = 2^(...) one exp2 pair in
-// kBwdPolyEvery takes the FMA-pipe polynomial instead of MUFU (0 = MUFU only).
-#ifndef FA_BWD_POLY_EVERY
-#define FA_BWD_POLY_EVERY 0
-#endif
-constexpr int kBwdPolyEvery = FA_BWD_POLY_EVERY;
-
-// Tuning knobs: compute warpgroups of the main kernel (2 or 4) at d = 64 and
-// d = 128; warpgroup g owns query columns [g 128/n, (g+1) 128/n) of every
-// tile.  More warpgroups hide more of the TMEM-load, MUFU and shared-memory
-// latency of the P and dS phases, at fewer registers per thread.
-#ifndef FA_BWD_DS_TMEM
-#define FA_BWD_DS_TMEM 0
-#endif
-// Tuning knob (d = 128): issue the dQ^T reductions of the previous query tile
-// interleaved with the dS loop, eight per chunk of eight queries (1), or all
-// at once after the partial is read from TMEM (0).
-#ifndef FA_BWD_DQ_INTERLEAVE
-#define FA_BWD_DQ_INTERLEAVE 1
-#endif
-// ... of which this many per thread go out at once (fewer values stay live
-// through the dS loop) and the rest spread evenly over its chunks.
-#ifndef FA_BWD_DQ_IMMEDIATE
-#define FA_BWD_DQ_IMMEDIATE 16
-#endif
-#ifndef FA_BWD_COMPUTE_WG_D64
-#define FA_BWD_COMPUTE_WG_D64 2
-#endif
-#ifndef FA_BWD_COMPUTE_WG_D128
-#define FA_BWD_COMPUTE_WG_D128 4
-#endif
-constexpr int kBwdPolyMod = kBwdPolyEvery > 0 ? kBwdPolyEvery : 1;  // divisor that is never zero
+// Compute warpgroups of the main kernel at d = 64 and d = 128; warpgroup g
+// owns query columns [g 128/n, (g+1) 128/n) of every tile.  More warpgroups
+// hide more of the TMEM-load, MUFU and shared-memory latency of the P and dS
+// phases, at fewer registers per thread.
+constexpr int kBwdComputeWgD64 = 2;
+constexpr int kBwdComputeWgD128 = 4;
+// d = 128: of a thread's dQ^T reductions of the previous query tile, this
+// many go out at once after the partial is read from TMEM; the rest are
+// spread evenly over the chunks of the next dS loop (fewer values stay live
+// through it, and the reductions overlap its arithmetic).
+constexpr int kBwdDqImmediate = 16;
 
 // ------------------------------------------------------------ preprocess ----
 // One warp per group of rows: 8 bf16 (16 bytes) per lane.
@@ -182,14 +153,13 @@ struct BwdCfg {
   // d = 64: a dedicated dQ warpgroup (the last four warps) drains each partial
   // through the staging buffers with tensor reduce-adds (asynchronous, so it
   // never waits on them); d = 128: the compute warpgroups drain it with
-  // coalesced reductions (FA_BWD_DQ_WARPGROUP selects the dedicated
-  // warpgroup there too; it measured slower).
-  static constexpr bool kDqWarpgroup = DQ && (!kDqTransposed || (FA_BWD_DQ_WARPGROUP != 0));
+  // coalesced reductions (a dedicated warpgroup measured slower there).
+  static constexpr bool kDqWarpgroup = DQ && !kDqTransposed;
   // d = 64: dK / dV leave through the dS buffer (free once the unit's last
   // MMAs are done) as two 64-column boxes with TMA stores; at d = 128 they
   // do not fit there and each thread stores its own row.
   static constexpr bool kEpiTma = (D == 64);
-  static constexpr int kWG = (D == 64) ? FA_BWD_COMPUTE_WG_D64 : FA_BWD_COMPUTE_WG_D128;  // compute warpgroups
+  static constexpr int kWG = (D == 64) ? kBwdComputeWgD64 : kBwdComputeWgD128;  // compute warpgroups
   static_assert(kWG == 2 || kWG == 4, "2 or 4 compute warpgroups");
   static constexpr int kQCols = kTileRows / kWG;  // query columns per compute warpgroup
   static constexpr int kDCols = D / kWG;          // dV / dK columns per compute warpgroup (epilogue)
@@ -205,12 +175,6 @@ struct BwdCfg {
   static constexpr int kColDV = 256;
   static constexpr int kColDK = 256 + D;
   static constexpr int kColDQ = !DQ ? 0 : kDqAliasesDp ? kColDP : 256 + 2 * D;
-  // d = 64 with FA_BWD_DS_TMEM: dS^T also packed as bf16 pairs in the last 64
-  // columns, so dK takes its A operand from TMEM instead of shared memory
-  // (d = 128 has no room).  Measured slower (the extra TMEM store sits on the
-  // compute warps' path), so off.
-  static constexpr bool kDsTmem = (D == 64) && (FA_BWD_DS_TMEM != 0);
-  static constexpr int kColDST = 256 + 3 * D;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKvStages * kTileBytes;
   static constexpr int kOffQ = kOffV + kKvStages * kTileBytes;    // [stages]
@@ -236,7 +200,6 @@ struct BwdCfg {
   static constexpr int kSmemBytes = kOffAbort + 4;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(!DQ || kColDQ + D <= kTmemCols, "tensor memory budget");
-  static_assert(!kDsTmem || (kColDST >= kColDQ + D && kColDST + 64 <= kTmemCols), "dS^T columns");
 };
 
 struct BwdUnit {
@@ -308,7 +271,6 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
   uint64_t* dqs_full = s_full + 12;  // d = 64: a dQ partial staged (128 arrivals)
   uint64_t* dqs_free = s_full + 13;  // d = 64: the staging buffer is free
   uint64_t* ds_empty2 = s_full + 14;  // second dS buffer (d = 64)
-  uint64_t* dst_empty = s_full + 15;  // dS^T in TMEM read by dK (d = 64)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
 
@@ -336,7 +298,6 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     mbar_init(ds_full, C::kComputeThreads);
     mbar_init(ds_empty, 1);
     mbar_init(ds_empty2, 1);
-    mbar_init(dst_empty, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, C::kDqWarpgroup ? 128 : C::kComputeThreads);
     mbar_init(dkdv_full, 1);
@@ -551,19 +512,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t dsb = ds_s + db * C::kDsBytes;
-          if (C::kDsTmem) {
-            // dK += dS^T Q with dS^T from TMEM (8 packed columns per 16 queries)
 #pragma unroll
-            for (int k = 0; k < kTileRows / 16; ++k)
-              mma_ts_w(tbase + C::kColDK, tbase + C::kColDST + 8 * k,
+          for (int k = 0; k < kTileRows / 16; ++k)
+            mma_ss_w(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
                      sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
-            mma_commit_w(dst_empty);  // dS^T in TMEM may be overwritten once dK(i) is done
-          } else {
-#pragma unroll
-            for (int k = 0; k < kTileRows / 16; ++k)
-              mma_ss_w(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
-                     sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
-          }
           mma_commit_w(&qdo_empty[st]);  // Q(i), dO(i) read for the last time: the producer may reload the slot
           if (C::kEarlyDp && x + 1 < u.nq) {
             tr(12);
@@ -620,7 +572,6 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + kQC * g);
     const uint32_t t_dv = tmem_lane_col(tbase, lanes, C::kColDV + kDC * g);
     const uint32_t t_dk = tmem_lane_col(tbase, lanes, C::kColDK + kDC * g);
-    const uint32_t t_dst = tmem_lane_col(tbase, lanes, C::kColDST + (kQC / 2) * g);  // packed dS^T (d = 64)
     // dS^T row r in shared memory: query q is 16-byte chunk q / 8 of the row,
     // in swizzle block (q / 8) / 8 at position (q / 8) % 8.
     const int chunk0 = kQC * g / 8;
@@ -629,13 +580,12 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     const int swz = r & 7;
     const uint64_t c2x2 = f2_pack(c2, c2);
     uint32_t scnt = 0, dpcnt = 0, dse = 0, ucnt = 0, qit = 0, dqcnt = 0;
-    uint32_t dstc = 0;        // d = 64: dS^T tiles written to TMEM
     uint32_t ecnt = 0;        // d = 64: units whose dK / dV went out through the dS buffer
     bool epi_pending = false;  // ... the last of which may still be reading it
     int pend_bh = 0, pend_qt = -1;  // dQ partial still to drain from the previous unit
     // (not with dropout: its keep bits leave no registers for the held values)
-    constexpr bool kDqInterleave = C::kDqTransposed && FA_BWD_DQ_INTERLEAVE != 0 && !DROP;
-    constexpr int kDqNow = FA_BWD_DQ_IMMEDIATE < kQC ? FA_BWD_DQ_IMMEDIATE : kQC;
+    constexpr bool kDqInterleave = C::kDqTransposed && !DROP;
+    constexpr int kDqNow = kBwdDqImmediate < kQC ? kBwdDqImmediate : kQC;
     constexpr int kDqPerChunk = (kQC - kDqNow) / (kQC / 8);  // the dS loop has kQC / 8 chunks
     static_assert(!kDqInterleave || kDqNow + kDqPerChunk * (kQC / 8) == kQC, "dQ reductions split");
 
@@ -681,7 +631,6 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         const int i = u.qtile(x);
         const int qbase = i * kTileRows + kQC * g;  // first query of this warpgroup's columns
         const bool diag = CAUSAL && (i == u.j);
-        const bool full_tile = (i + 1) * kTileRows <= N;  // no padded queries (their P must stay exactly 0)
         // -lse2 / -D of this query tile, staged in shared memory with Q / dO
         const float* rows =
             reinterpret_cast<const float*>(sm + C::kOffRow + (qit % C::kStages) * C::kRowBytes) + kQC * g;
@@ -730,15 +679,9 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           for (int e = 0; e < 16; ++e) {
             const uint64_t nl2 = (e & 1) ? nlv[e / 2].y : nlv[e / 2].x;
             const uint64_t xx = f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2x2, nl2);
-            float p0, p1;
-            if (kBwdPolyEvery > 0 && full_tile && (e % kBwdPolyMod) == kBwdPolyMod - 1) {
-              f2_unpack(ex2_poly2(xx), p0, p1);
-            } else {
-              float x0, x1;
-              f2_unpack(xx, x0, x1);
-              p0 = ex2(x0);
-              p1 = ex2(x1);
-            }
+            float x0, x1;
+            f2_unpack(xx, x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
             if (diag) {
               const int q = qbase + 32 * c + 2 * e;
               if (q < kr) p0 = 0.f;
@@ -768,7 +711,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         mbar_arrive(p_full);
         tr(3);
         // ---- dQ partial of the previous query tile ----
-        // d = 128 with FA_BWD_DQ_INTERLEAVE: the drained dQ^T column piece
+        // d = 128 (without dropout): the drained dQ^T column piece
         // waiting for its reductions (issued by this tile's dS loop)
         uint32_t dqv[kDqInterleave ? kQC : 1];
         float* dq_dst = dq_acc;
@@ -864,7 +807,6 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
               float d0, d1;
               f2_unpack(f2_mul(f2_pack(pf.x, pf.y), t), d0, d1);
               dsk[e] = pack_bf16x2(d0, d1);
-              if (C::kDsTmem) pk[idx] = dsk[e];  // P^T is no longer needed: keep dS^T for TMEM
             }
             *reinterpret_cast<uint4*>(ds_row + (((cbase + m) ^ swz) * 16)) = make_uint4(dsk[0], dsk[1], dsk[2], dsk[3]);
             if (kDqInterleave && dq_have) {  // the rest, kDqPerChunk per chunk of eight queries
@@ -875,16 +817,6 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
               }
             }
           }
-        }
-        if (C::kDsTmem) {
-          // dS^T also into TMEM (the A operand of dK), once dK of the previous
-          // tile has read it there.
-          if (!(ok = mbar_wait_warp(dst_empty, (dstc & 1) ^ 1, status))) break;
-          ++dstc;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < kQC / 32; ++c) tmem_st16(t_dst + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
-          tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -986,10 +918,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     if (C::kEpiTma && warp == 0 && lane == 0) tma_store_wait_all0();
   } else if (C::kDqWarpgroup) {
     // ----------------------------------------------------- dQ warpgroup --
-    // d = 128 (transposed partial): thread = head-dimension index r; it reads
-    // the whole dQ^T row (128 queries), releases the columns, then reduces it
-    // into the accumulator (per query a warp covers 128 contiguous bytes).
-    // d = 64: thread = query row r; it reads its 64-column dQ row, releases
+    // d = 64 only: thread = query row r; it reads its 64-column dQ row, releases
     // the columns, writes the row into a pair of 128-byte-swizzled 32-column
     // boxes, and one thread issues the tensor reduce-adds.
     const int quarter = warp % 4;
@@ -1010,21 +939,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         ++qcnt;
         if (!ok) break;
         tc_fence_after();
-        if (C::kDqTransposed) {
-          uint32_t v[128];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(t_dq + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(dq_empty);
-          tr(41);
-          const int q0 = u.qtile(x) * kTileRows;
-          const int nvalid = N - q0;
-          float* dst = dq_acc + ((size_t)u.bh * N + q0) * D + r;
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < nvalid) red_add(dst + (size_t)c * D, __uint_as_float(v[c]));
-        } else {
+        {
           uint8_t* stage = sm + C::kOffDQS;
           if (elected) {
             tma_store_wait_read0();  // the previous reduce-adds have read the buffer

@@ -49,16 +49,6 @@
 
 namespace fa {
 
-// Tuning knob: one exp2 pair in kPolyEvery takes the FMA-pipe polynomial
-// instead of MUFU (0 = MUFU only).  Measured on GB300, every fraction tried
-// (1/2, 1/4, 1/8) was slower than MUFU alone: the softmax is bound by issue
-// and latency, not by the MUFU rate, so the default is 0.
-#ifndef FA_FWD_POLY_EVERY
-#define FA_FWD_POLY_EVERY 0
-#endif
-constexpr int kPolyEvery = FA_FWD_POLY_EVERY;
-constexpr int kPolyMod = kPolyEvery > 0 ? kPolyEvery : 1;  // divisor that is never zero
-
 #ifdef FA_TEST_HOOKS
 // Test builds only (-DFA_TEST_HOOKS, never the default library): when set,
 // softmax warpgroup 0 withholds its first "P ready" arrival of every unit, so
@@ -622,13 +612,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::threads(PVW), 1)
           }
         }
         tr(4);
-        // P = 2^(s c2 - m_run) in pairs, summed in fp32, stored as bf16 pairs over
-        // S_t in four 16-column pieces.  One pair in four takes the FMA-pipe
-        // polynomial instead of MUFU (unmasked tiles only, so masked entries
-        // stay exactly 0).
+        // P = 2^(s c2 - m_run) in pairs, summed in fp32, stored as bf16 pairs
+        // (over S_t at d = 128) in four 16-column pieces.
         const uint64_t c2x2 = f2_pack(c2, c2);
         const uint64_t negm = f2_pack(-m_run, -m_run);
-        const bool use_poly = !(tail || diag);
         uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};  // partial row sums (pairs)
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -638,14 +625,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::threads(PVW), 1)
           for (int i = 0; i < 16; ++i) {
             const int c = 32 * h + 2 * i;
             const uint64_t x = f2_fma(f2_pack(s[c], s[c + 1]), c2x2, negm);
-            uint64_t p;
-            if (kPolyEvery > 0 && use_poly && (i % kPolyMod) == kPolyMod - 1) {
-              p = ex2_poly2(x);
-            } else {
-              float x0, x1;
-              f2_unpack(x, x0, x1);
-              p = f2_pack(ex2(x0), ex2(x1));
-            }
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            const uint64_t p = f2_pack(ex2(x0), ex2(x1));
             ls[i & 3] = f2_add(ls[i & 3], p);
             float p0, p1;
             f2_unpack(p, p0, p1);

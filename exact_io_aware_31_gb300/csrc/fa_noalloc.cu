@@ -8,9 +8,8 @@
 // exactly the kernels of fa_bwd with that array as the workspace.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/fa.h"
+#include "fa_context.h"
 
 namespace fa {
 namespace {
@@ -19,29 +18,16 @@ namespace {
 // device symbol: host code must pass the address cudaGetSymbolAddress returns.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
+// Its device address, looked up with cudaGetSymbolAddress on the first call
+// in each context (with that context's device current) and cached by the
+// context's unique ID: an address from one context is not valid in another,
+// nor in a primary context created again after a reset.
+PerContextAddress g_noalloc_addr;
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
 int noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    cudaGetLastError();
-    return FA_ERR_CUDA;
-  }
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return FA_ERR_CUDA;
-    }
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
-  return FA_OK;
+  return g_noalloc_addr.get(out, [](void** p) { return cudaGetSymbolAddress(p, g_noalloc_scratch); }) == 0
+             ? FA_OK
+             : FA_ERR_CUDA;
 }
 
 }  // namespace
@@ -50,9 +36,14 @@ int noalloc_scratch(void** out) {
 extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                               float scale, int causal, cudaStream_t stream) {
+  // Validate every argument exactly as fa_bwd does before looking at the size:
+  // fa_bwd checks sizes, scale, mask flag and pointers ahead of its workspace
+  // and, given none, returns without touching the device.  FA_ERR_WORKSPACE
+  // from this call therefore means every other argument is valid.
   const size_t need = fa_bwd_workspace_size(B, H, N, d);
-  if (need == 0)  // invalid sizes: let fa_bwd report which, before any device work
-    return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, nullptr, 0, stream);
+  const int arg = fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, nullptr,
+                         need ? need : 1, nullptr);
+  if (arg != FA_ERR_WORKSPACE) return arg;
   if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int st = fa::noalloc_scratch(&scratch);

@@ -9,8 +9,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
-#include "exp2_poly.h"
-
 namespace fa {
 
 // ---------------------------------------------------------------- errors ----
@@ -90,30 +88,16 @@ __device__ __forceinline__ bool mbar_probe(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
-// Tuning knob: the spin of the bounded waits below tests with try_wait (0,
-// may suspend the thread until the phase completes) or with the
-// non-blocking test_wait (1, pure polling).
-#ifndef FA_WAIT_POLL
-#define FA_WAIT_POLL 0
-#endif
-__device__ __forceinline__ bool mbar_spin_test(uint32_t addr, uint32_t parity) {
-#if FA_WAIT_POLL
-  return mbar_probe(addr, parity);
-#else
-  return mbar_test(addr, parity);
-#endif
-}
-
 // Wait until the phase with the given parity has completed.  Returns false
 // (after recording kDevTimeout in *status) if it has not within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
   const uint32_t a = smem_addr(bar);
-  if (mbar_spin_test(a, parity)) return true;
+  if (mbar_test(a, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_spin_test(a, parity)) return true;
+      if (mbar_test(a, parity)) return true;
     if (global_ns() - t0 > kWaitLimitNs) {
       atomicExch(status, kDevTimeout);
       return false;
@@ -127,13 +111,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 // broadcast, so a timeout is also warp-uniform.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status) {
   const uint32_t a = smem_addr(bar);
-  bool done = mbar_spin_test(a, parity);
+  bool done = mbar_test(a, parity);
   if (__all_sync(0xffffffffu, done)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i) {
-      done = done || mbar_spin_test(a, parity);
+      done = done || mbar_test(a, parity);
       if (__all_sync(0xffffffffu, done)) return true;
     }
     const bool expired = __shfl_sync(0xffffffffu, (global_ns() - t0 > kWaitLimitNs) ? 1 : 0, 0) != 0;
@@ -425,30 +409,6 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
-}
-
-// 2^x on the FMA pipe for a pair of arguments, x <= 126 (see exp2_poly.h):
-// j = round(x) through the 1.5 * 2^23 shift, f = x - j in [-1/2, 1/2],
-// p(f) ~ 2^f (relative error < 7.5e-5), then j added to p's exponent field.
-// Arguments below -125 are clamped there (result ~2^-125 instead of ~0).
-__device__ __forceinline__ uint64_t ex2_poly2(uint64_t x) {
-  float x0, x1;
-  f2_unpack(x, x0, x1);
-  x0 = fmaxf(x0, -125.f);
-  x1 = fmaxf(x1, -125.f);
-  const uint64_t shift = f2_pack(12582912.f, 12582912.f);
-  const uint64_t xc = f2_pack(x0, x1);
-  const uint64_t t = f2_add(xc, shift);
-  const uint64_t j = f2_add(t, f2_pack(-12582912.f, -12582912.f));
-  const uint64_t f = f2_fma(j, f2_pack(-1.f, -1.f), xc);  // x - j
-  uint64_t p = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
-  p = f2_fma(p, f, f2_pack(kExp2C1, kExp2C1));
-  p = f2_fma(p, f, f2_pack(kExp2C0, kExp2C0));
-  float p0, p1, t0, t1;
-  f2_unpack(p, p0, p1);
-  f2_unpack(t, t0, t1);
-  return f2_pack(__int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23)),
-                 __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23)));
 }
 
 // Pack two floats to bf16x2 (round to nearest even): `lo` in bits 0..15.

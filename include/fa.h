@@ -241,12 +241,20 @@ int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, const v
  * device array of FA_NOALLOC_SCRATCH_BYTES owned by the library, and nothing
  * is allocated or freed by the call.
  *
- *   Limit     fa_bwd_workspace_size(B, H, N, d) must not exceed
- *             FA_NOALLOC_SCRATCH_BYTES; larger sizes return FA_ERR_WORKSPACE
- *             without launching anything (e.g. B*H*N*d up to ~16M elements).
- *   Set-up    the first call on each device looks up the scratch's device
- *             address (cudaGetSymbolAddress) with that device current; make
- *             that first call before any stream capture.
+ *   Limit     exactly fa_bwd_workspace_size(B, H, N, d) <=
+ *             FA_NOALLOC_SCRATCH_BYTES, where that size is
+ *             round256(4 B H N d) + 2 round256(4 B H Npad) bytes, Npad = N
+ *             rounded up to a multiple of 128 (for example B = 2, H = 8,
+ *             N = 8064, d = 128 fits with 16 KiB to spare; N = 8065 does
+ *             not).  Larger problems return FA_ERR_WORKSPACE without
+ *             launching anything; invalid arguments are reported first, with
+ *             fa_bwd's codes.
+ *   Set-up    the first call in each CUDA context looks up the scratch's
+ *             device address (cudaGetSymbolAddress) with that context and
+ *             its device current, and caches it by the context's unique ID
+ *             (another context, or a primary context created again after a
+ *             reset, looks it up anew); make that first call before any
+ *             stream capture.
  *   Sharing   every call on a device uses the same scratch, which keeps the
  *             last call's contents (the call itself clears what must start at
  *             zero).  Calls that overlap on the GPU (different streams, no

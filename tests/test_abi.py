@@ -230,3 +230,33 @@ def test_bwd_dq_convert_validation(lib, kw, code):
     args = dict(dq=A, B=1, H=1, N=16, d=64, scale=0.125, workspace=A, workspace_bytes=1 << 30, stream=None)
     args.update(kw)
     assert fa.fa_bwd_dq_convert(**args) == code
+
+
+# Oversized for the 64 MiB scratch of fa_bwd_noalloc (a 128 MiB dQ accumulator).
+BIG = dict(B=1, H=64, N=4096, d=128)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), fa.FA_ERR_WORKSPACE),                        # valid, too large: refused before any device work
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),            # bad arguments are named as such, whatever the size
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(dq=A + 4), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=1, H=1, N=16, d=96), fa.FA_ERR_UNSUPPORTED),
+])
+def test_noalloc_validates_arguments_before_its_size_limit(lib, kw, code):
+    args = dict(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, **BIG, scale=0.1, causal=0, stream=None)
+    args.update(kw)
+    assert fa.fa_bwd_noalloc(**args) == code
+
+
+def test_noalloc_limit_is_the_workspace_size(lib):
+    """B2 H8 N8064 d128 fits the 64 MiB scratch (16 KiB to spare); one more row does not (refused on the CPU)."""
+    assert fa.NOALLOC_SCRATCH_BYTES - (16 << 10) == fa.fa_bwd_workspace_size(2, 8, 8064, 128)
+    assert fa.fa_bwd_workspace_size(2, 8, 8065, 128) > fa.NOALLOC_SCRATCH_BYTES
+    args = dict(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, B=2, H=8, N=8065, d=128, scale=0.1, causal=1,
+                stream=None)
+    assert fa.fa_bwd_noalloc(**args) == fa.FA_ERR_WORKSPACE
