@@ -84,23 +84,23 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-# The device code of each profiled kernel: its translation unit and the device
-# headers it includes (host-side launch plumbing is not part of it).
+# The translation unit of each profiled kernel; its hash covers that file and
+# every header it includes (followed through #include, as the build does).
 KERNEL_SOURCES = {
-    "fa_fwd_kernel": ["fa_fwd.cu"],
-    "fa_fwd_kernel_fp8": ["fa_fwd.cu"],
-    "fa_bwd_pre": ["fa_bwd.cu"],
-    "fa_bwd_main": ["fa_bwd.cu"],
-    "fa_bwd_dq_conv": ["fa_bwd.cu"],
+    "fa_fwd_kernel": "fa_fwd.cu",
+    "fa_fwd_kernel_fp8": "fa_fwd.cu",
+    "fa_bwd_pre": "fa_bwd.cu",
+    "fa_bwd_main": "fa_bwd.cu",
+    "fa_bwd_dq_conv": "fa_bwd.cu",
 }
-DEVICE_HEADERS = ["fa_common.cuh", "fa_dropout.cuh", "sm103_ptx.cuh", "exp2_poly.h"]
 
 
 def source_hash(kernel):
+    from exact_io_aware_31_gb300 import build
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kernel] + DEVICE_HEADERS:
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    for path in build.build_inputs(CSRC, (KERNEL_SOURCES[kernel],)):
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -170,24 +170,56 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def oracle_sample(w, q, k, v, do, seconds):
-    """Time the fp64 oracle (forward + backward) on whole (b, h) slices for about `seconds`."""
-    import oracle
+ORACLE_ROWS = 1024  # query rows per oracle sample unit
+
+
+def oracle_units(w):
+    """Sample units of the workload for the CPU oracle: (slice b, slice h, first row, rows).
+
+    A unit is one block of up to ORACLE_ROWS query rows of one (b, h) slice,
+    forward and (for workloads with a backward) that block's whole share of
+    the backward: its dQ rows and its terms of dK and dV.  Units are visited
+    spread over slices and row blocks, in a fixed order."""
+    nblk = (w.N + ORACLE_ROWS - 1) // ORACLE_ROWS
+    units = []
+    for i in range(w.B * w.H * nblk):
+        sl = i % (w.B * w.H)
+        blk = (i // (w.B * w.H) + 7 * sl) % nblk
+        b, h = divmod(sl, w.H)
+        r0 = blk * ORACLE_ROWS
+        units.append((b, h, r0, min(ORACLE_ROWS, w.N - r0)))
+    return units
+
+
+def oracle_unit_flops(w, rows):
+    """The metric's FLOPs (fwd + bwd) carried by `rows` query rows of one slice."""
     fwd, bwd = flops_per_step(w)
-    per_slice = (fwd + bwd) / (w.B * w.H)
-    done, t0 = 0, time.perf_counter()
+    return (fwd + bwd) * rows / (w.B * w.H * w.N)
+
+
+def oracle_run_unit(w, q, k, v, do, unit):
+    import oracle
+    b, h, r0, rows = unit
+    qd, kd, vd, dod = (t[b, h].double().numpy() for t in (q, k, v, do))
+    if w.backward:
+        oracle.attention_backward_head_rows(qd, kd, vd, dod, range(r0, r0 + rows), w.scale, w.causal)
+    else:
+        oracle.attention_forward_head_rows(qd, kd, vd, range(r0, r0 + rows), w.scale, w.causal)
+
+
+def oracle_sample(w, q, k, v, do, seconds, start=0):
+    """Time the fp64 oracle on sample units (at least one) for about `seconds`: (TFLOP/s, units, s)."""
+    units = oracle_units(w)
+    done, flops, t0 = 0, 0.0, time.perf_counter()
     while True:
-        b, h = divmod(done % (w.B * w.H), w.H)
-        qd, kd, vd, dod = (t[b, h].double().numpy() for t in (q, k, v, do))
-        if w.backward:
-            oracle.attention_backward_head(qd, kd, vd, dod, w.scale, w.causal)
-        else:
-            oracle.attention_forward_head_rows(qd, kd, vd, range(w.N), w.scale, w.causal)
+        unit = units[(start + done) % len(units)]
+        oracle_run_unit(w, q, k, v, do, unit)
+        flops += oracle_unit_flops(w, unit[3])
         done += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return done * per_slice / el / 1e12, done, el
+    return flops / el / 1e12, done, el
 
 
 def cores():
@@ -198,23 +230,35 @@ def cores():
 
 
 def run_reference(args, w):
+    """The fp64 CPU oracle on the host cores; each step is one bounded sample unit of the workload.
+
+    ``ms_per_step`` is the measured mean time of those sampled steps;
+    ``extrapolated_ms_per_workload_step`` scales it to the whole workload by
+    the metric's FLOPs and is not a measurement."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     q, k, v, do = workloads.workload_inputs(w)
-    vals = []
+    units = oracle_units(w)
+    times, flops = [], []
     for i in range(args.warmup + args.steps):
-        val, n, el = oracle_sample(w, q, k, v, do, args.ref_seconds)
+        unit = units[i % len(units)]
+        t0 = time.perf_counter()
+        oracle_run_unit(w, q, k, v, do, unit)
+        el = time.perf_counter() - t0
         if i >= args.warmup:
-            vals.append((val, n, el))
-    value = statistics.median(v for v, _, _ in vals)
+            times.append(el)
+            flops.append(oracle_unit_flops(w, unit[3]))
+    value = sum(flops) / sum(times) / 1e12
     fwd, bwd = flops_per_step(w)
-    sample = (f"whole (b,h) slices of the workload, fwd{'+bwd' if w.backward else ''} in fp64 numpy, "
-              f"about {args.ref_seconds:.0f} s per step ({vals[-1][1]} slices of {w.B * w.H} in the last)")
+    ms = 1e3 * sum(times) / len(times)
+    sample = (f"each step one unit of up to {ORACLE_ROWS} query rows of one (b,h) slice (fwd"
+              f"{' + its whole share of the bwd' if w.backward else ''}) in fp64 numpy, units spread over "
+              f"slices and row blocks; {len(times)} timed steps, {sum(times):.1f} s")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * (fwd + bwd) / (value * 1e12), 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "extrapolated_ms_per_workload_step": round(1e3 * (fwd + bwd) / (value * 1e12), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {**w.describe(), "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores(), "kind": "oracle",
                              "sample": sample},
@@ -390,6 +434,32 @@ def run_ours(args, w):
     e2e_value = whole_job_tflops(world, fwd_f + bwd_f, e2e_ms)
     check(fa.fa_get_device_status(cmp_h), "e2e")
 
+    # ---- the copies' own ceiling on this host: the same tensors moved with no
+    # kernels, each direction alone and both at once (the e2e loop overlaps them)
+    def copies(h2d_on, d2h_on, n):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        c0.record(s_in)
+        s_out.wait_event(c0)
+        for i in range(n):
+            st = i % n_sets
+            if h2d_on:
+                with torch.cuda.stream(s_in):
+                    for hd, dd in ((hq, dev_in[st][0]), (hk, dev_in[st][1]), (hv, dev_in[st][2])) + (
+                            ((hdo, dev_in[st][3]),) if w.backward else ()):
+                        dd.copy_(hd, non_blocking=True)
+            if d2h_on:
+                with torch.cuda.stream(s_out):
+                    for hd, dd in zip(host_out[st][:n_out], dev_out[st][:n_out]):
+                        hd.copy_(dd, non_blocking=True)
+        s_in.wait_stream(s_out)
+        c1.record(s_in)
+        torch.cuda.synchronize()
+        return c0.elapsed_time(c1) / n
+    copies(True, True, 1)
+    h2d_ms, d2h_ms, both_ms = copies(True, False, e2e_steps), copies(False, True, e2e_steps), copies(True, True, e2e_steps)
+    e2e_ceiling = whole_job_tflops(world, fwd_f + bwd_f, max(ms_per_step, both_ms))
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -397,6 +467,16 @@ def run_ours(args, w):
 
     # ---- roofline of the dominant kernel ----
     peaks, peak_src = load_peaks()
+    # Each pass against the measured dense bf16 peak (burst): the forward is its
+    # one launch, the backward its three (preprocess, main, dQ convert).
+    fwd_ms = kern_avg["fa_fwd_kernel"]
+    bwd_ms = sum(kern_avg[k_] for k_ in ("fa_bwd_pre", "fa_bwd_main", "fa_bwd_dq_conv") if k_ in kern_avg)
+    pass_fracs = {"fwd_ms": round(fwd_ms, 4), "fwd_tflops": round(fwd_f / (fwd_ms * 1e-3) / 1e12, 1),
+                  "fwd_frac": round(fwd_f / (fwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+    if w.backward:
+        pass_fracs.update({"bwd_ms": round(bwd_ms, 4), "bwd_tflops": round(bwd_f / (bwd_ms * 1e-3) / 1e12, 1),
+                           "bwd_frac": round(bwd_f / (bwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)})
+    pass_fracs["frac_peak"] = f"{peaks['bf16_tflops']} TFLOP/s, {peak_src} dense bf16 (burst)"
     dom = max(kern_avg, key=kern_avg.get)
     per_launch = {"fa_fwd_kernel": fwd_f, "fa_bwd_main": bwd_f}
     if dom in per_launch:
@@ -425,18 +505,26 @@ def run_ours(args, w):
                        "l2": ("flushed between steps (2x L2 buffer written)" if flush
                               else "inputs larger than L2 (each tensor > 129 MB)"),
                        "fwd_tflop_per_step": round(fwd_f / 1e12, 4), "bwd_tflop_per_step": round(bwd_f / 1e12, 4),
+                       **pass_fracs,
                        "pct_of_dense_bf16_2250": round(100 * value / world / 2250.0, 2),
                        "pct_of_measured_bf16": round(100 * value / world / peaks["bf16_tflops"], 2)},
             "roofline": roof, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
             "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "pipelining": "2 device buffer sets; step k+1's host-to-device and step k-1's "
-                                  "device-to-host copies overlap step k's kernels"}}
+                                  "device-to-host copies overlap step k's kernels",
+                    "copy_gbs_ceiling": {"h2d_alone": round(h2d / (h2d_ms * 1e-3) / 1e9, 1),
+                                         "d2h_alone": round(d2h / (d2h_ms * 1e-3) / 1e9, 1),
+                                         "both_at_once_ms_per_step": round(both_ms, 4)},
+                    "ceiling": round(e2e_ceiling, 3),
+                    "ceiling_is": "the metric at max(device step, both directions' copies at once)",
+                    "frac_of_ceiling": round(e2e_value / e2e_ceiling, 4)}}
     if world == 1 and not args.no_cpu_baseline:
         val, n, el = oracle_sample(w, q, k, v, do, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(val, 6), "unit": UNIT, "cores": cores(), "kind": "oracle",
-                                "sample": f"{n} whole (b,h) slice(s) of {w.B * w.H}, fwd"
-                                          f"{'+bwd' if w.backward else ''} in fp64 numpy, {el:.1f} s"}
+                                "sample": f"{n} unit(s) of up to {ORACLE_ROWS} query rows of one (b,h) slice "
+                                          f"(fwd{' + its share of the bwd' if w.backward else ''}) of "
+                                          f"{len(oracle_units(w))} in the workload, fp64 numpy, {el:.1f} s"}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -666,18 +754,14 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=workloads.GPT2_MEDIUM.name,
+    ap.add_argument("--workload", default=workloads.LONG_SEQ.name,
                     help="one of: " + ", ".join(sorted(workloads.BY_NAME) + sorted(workloads.DECODE_BY_NAME)))
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
-    ap.add_argument("--ref-seconds", type=float, default=None,
-                    help="oracle time per step for --impl reference (default: 150 s spread over all steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true", help="forward with E4M3 Q, K (fa_fwd_fp8) on a d = 128 workload")
     args = ap.parse_args()
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
-    if args.ref_seconds is None:
-        args.ref_seconds = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
     if args.workload in workloads.DECODE_BY_NAME:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the forward/backward "

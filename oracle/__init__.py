@@ -22,6 +22,7 @@ PyTorch's own fp64 ``scaled_dot_product_attention`` and autograd, SciPy's
 from .attention import (  # noqa: F401
     attention_backward,
     attention_backward_head,
+    attention_backward_head_rows,
     attention_forward,
     attention_forward_head_rows,
     attention_forward_tiled,

@@ -33,6 +33,7 @@ __all__ = [
     "attention_forward_tiled",
     "attention_backward",
     "attention_backward_head",
+    "attention_backward_head_rows",
 ]
 
 _DEFAULT_ROW_BLOCK = 1024
@@ -243,3 +244,31 @@ def attention_backward(q, k, v, do, scale, causal, row_block=_DEFAULT_ROW_BLOCK)
             dq[bi, hi], dk[bi, hi], dv[bi, hi], D[bi, hi], _, _ = attention_backward_head(
                 q[bi, hi], k[bi, hi], v[bi, hi], do[bi, hi], scale, causal, row_block)
     return dq, dk, dv, D
+
+
+def attention_backward_head_rows(q, k, v, do, rows, scale, causal):
+    """What query ``rows`` of ONE head contribute to the gradients: ``(dq_rows, dk_part, dv_part)``.
+
+    The formulas of :func:`attention_backward_head` evaluated for the asked
+    rows only.  Row i's forward output, logsumexp, D_i and dS row depend on
+    row i alone (and on every key and value), so ``dq_rows`` is exactly those
+    rows of dQ, while dK and dV are sums over query rows: ``dk_part`` and
+    ``dv_part`` are the asked rows' terms, and summing them over a partition of
+    all rows gives dK and dV.  Lets a bounded sample of a large workload be
+    timed or checked without the whole head.
+    """
+    q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
+    rows = np.asarray(rows)
+    o_r, lse_r = attention_forward_head_rows(q, k, v, rows, scale, causal)
+    D = np.sum(do[rows] * o_r, axis=1)
+    s = scale * (q[rows] @ k.T)
+    if causal:
+        j = np.arange(k.shape[0])[None, :]
+        s = np.where(j > rows[:, None], -np.inf, s)
+    p = np.exp(s - lse_r[:, None])                         # recomputed P rows
+    dv_part = p.T @ do[rows]
+    dp = do[rows] @ v.T
+    ds = p * (dp - D[:, None])
+    dq_rows = scale * (ds @ k)
+    dk_part = scale * (ds.T @ q[rows])
+    return dq_rows, dk_part, dv_part

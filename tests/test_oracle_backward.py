@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import attention_backward, attention_backward_head, attention_forward
+from oracle import attention_backward, attention_backward_head, attention_backward_head_rows, attention_forward
 
 
 def _rand(shape, seed, scale=1.0):
@@ -92,3 +92,25 @@ def test_batched_backward_equals_per_head():
             hq, hk, hv, hD, _, _ = attention_backward_head(q[b, h], k[b, h], v[b, h], do[b, h], 0.5, True)
             assert np.array_equal(hq, dq[b, h]) and np.array_equal(hk, dk[b, h])
             assert np.array_equal(hv, dv[b, h]) and np.array_equal(hD, D[b, h])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_contributions_match_torch_autograd(causal):
+    """dQ rows are autograd's rows; dK, dV contributions summed over a partition of the rows are autograd's."""
+    n, d = 150, 16
+    q, k, v, do = (_rand((n, d), s) for s in (141, 142, 143, 144))
+    scale = 0.4
+    tq, tk, tv = (torch.from_numpy(a.copy()).requires_grad_(True) for a in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(tq[None, None], tk[None, None], tv[None, None],
+                                                           is_causal=causal, scale=scale)
+    out.backward(torch.from_numpy(do)[None, None])
+    dk_sum, dv_sum = np.zeros_like(k), np.zeros_like(v)
+    order = np.random.default_rng(5).permutation(n)
+    for part in (order[:37], order[37:90], order[90:]):
+        dq_r, dk_p, dv_p = attention_backward_head_rows(q, k, v, do, part, scale, causal)
+        assert np.max(np.abs(dq_r - tq.grad.numpy()[part])) < 1e-11
+        dk_sum += dk_p
+        dv_sum += dv_p
+    assert np.max(np.abs(dk_sum - tk.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dv_sum - tv.grad.numpy())) < 1e-11
+
