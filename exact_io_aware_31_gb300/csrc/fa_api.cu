@@ -133,7 +133,7 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 int check_sizes(int B, int H, int N, int d, float scale, int causal) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   const long long bh = (long long)B * H;
   if (bh > INT_MAX || (long long)N > (1 << 30)) return FA_ERR_INVALID_ARG;
   const long long npad = ((long long)N + 127) / 128 * 128;
@@ -144,13 +144,14 @@ int check_sizes(int B, int H, int N, int d, float scale, int causal) {
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// scale * log2(e), floored at 1e-30 so that a masked score (-inf) times it
-// stays -inf when scale == 0.  For finite scores |s| < 1e8 the floor changes
-// 2^(s * c2) by less than one fp32 ulp of 1, so scale == 0 still gives exact
-// uniform attention.
+// scale * log2(e), its magnitude floored at 1e-30 so that a masked score
+// (-inf) times |c2| stays -inf when scale == 0.  For finite scores |s| < 1e8
+// the floor changes 2^(s * c2) by less than one fp32 ulp of 1, so scale == 0
+// still gives exact uniform attention.  The sign is kept: the tensor-core
+// kernels compute S negated for a negative scale and use |c2| after it.
 float log2_scale(float scale) {
   const float c2 = scale * 1.4426950408889634f;
-  return c2 > 1e-30f ? c2 : 1e-30f;
+  return std::fabs(c2) > 1e-30f ? c2 : std::copysign(1e-30f, c2);
 }
 
 struct WorkspaceLayout {
@@ -220,7 +221,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o
                           int d, float scale, float q_descale, float k_descale, int causal, cudaStream_t stream) {
   int st = check_sizes(B, H, N, d, scale, causal);
   if (st != FA_OK) return st;
-  if (!std::isfinite(q_descale) || !std::isfinite(k_descale) || q_descale < 0.f || k_descale < 0.f)
+  if (!std::isfinite(q_descale) || !std::isfinite(k_descale) || q_descale < 0.f || k_descale < 0.f || scale < 0.f)
     return FA_ERR_INVALID_ARG;
   const float eff = scale * q_descale * k_descale;
   if (!std::isfinite(eff)) return FA_ERR_INVALID_ARG;
@@ -244,7 +245,7 @@ constexpr int kMaxDecodeQueries = 8;
 int check_decode(int B, int H, int Nq, int Nk, int d, float scale, int causal, int num_splits) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   const long long bh = (long long)B * H;
   if (bh > INT_MAX || (long long)Nk > (1 << 30)) return FA_ERR_INVALID_ARG;
   const long long kpad = ((long long)Nk + 127) / 128 * 128;

@@ -246,6 +246,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int N, int Npad, float c2,
                 float scale, DropParams dp, int* status) {
   using C = BwdCfg<D, DQ>;
+  // A negative scale arrives as a negative c2: S^T is computed negated (K
+  // negated as the A operand) and P uses |c2|; dK and dQ take the signed scale.
+  const uint32_t s_negate = c2 < 0.f ? kIdescNegateA : 0u;
+  c2 = fabsf(c2);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
   uint8_t* sm = smem_raw;
@@ -417,6 +421,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     // ---------------------------------------------------------- MMA issuer --
     {  // whole warp, converged: waits are warp-wide, one elected lane issues
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T: both K-major over d
+      const uint32_t idST = kIdSS | s_negate;                  // S^T = (+/-) K Q^T
       constexpr uint32_t kIdKV = idesc_bf16(128, D, 0, 1);    // dV, dK: B (dO / Q) MN-major
       constexpr uint32_t kIdQ = idesc_bf16(128, C::kDqTransposed ? 128 : D, 1, 1);  // dQ / dQ^T: A, B MN-major
       const uint32_t q_s = smem_addr(sm + C::kOffQ);
@@ -438,7 +443,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
             mma_ss_w(tbase + C::kColS, sdesc(kmajor(k_s, k), 16, 1024),
-                   sdesc(kmajor(q_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
+                   sdesc(kmajor(q_s + st * C::kTileBytes, k), 16, 1024), idST, k > 0);
           mma_commit_w(s_full);
         };
         auto issue_dp = [&](int st) {  // dP^T = V dO^T

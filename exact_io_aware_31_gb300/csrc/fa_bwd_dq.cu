@@ -81,6 +81,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
               const float* __restrict__ lse2, const float* __restrict__ dsum, __nv_bfloat16* __restrict__ dq, int BH,
               int N, int Npad, float c2, float scale, int* status) {
   using C = DqCfg<D>;
+  // A negative scale arrives as a negative c2: S is computed negated (Q
+  // negated as the A operand), the exponentials use |c2|, dQ the signed scale.
+  const uint32_t s_negate = c2 < 0.f ? kIdescNegateA : 0u;
+  c2 = fabsf(c2);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
   uint8_t* sm = smem_raw;
@@ -184,6 +188,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     // ---------------------------------------------------------- MMA issuer --
     {  // whole warp, converged: waits are warp-wide, one elected lane issues
       constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // S, dP: A and B K-major over d
+      const uint32_t idS = kIdS | s_negate;                   // S = (+/-) Q K^T
       constexpr uint32_t kIdQ = idesc_bf16(128, D, 0, 1);    // dQ += dS K: A from TMEM, B (K) MN-major
       auto kmajor = [](uint32_t base, int k) { return base + (k / 4) * kSwzBlockBytes + (k % 4) * 32; };
       uint32_t ucnt = 0, kvit = 0, dscnt = 0, dqcnt = 0;
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           // dQ of the previous key tile, issued before these)
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(tbase + C::kColS, sdesc(kmajor(q_s, k), 16, 1024), sdesc(kmajor(k_s, k), 16, 1024), kIdS, k > 0);
+            mma_ss_w(tbase + C::kColS, sdesc(kmajor(q_s, k), 16, 1024), sdesc(kmajor(k_s, k), 16, 1024), idS, k > 0);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
             mma_ss_w(tbase + C::kColDP, sdesc(kmajor(do_s, k), 16, 1024), sdesc(kmajor(v_s, k), 16, 1024), kIdS,

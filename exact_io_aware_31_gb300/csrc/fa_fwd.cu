@@ -155,6 +155,11 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::threads(PVW), 1)
                   float* __restrict__ lse, int BH, int N, float c2, DropParams dp, int* status) {
   using C = FwdCfg<D, F8>;
   static_assert(!PVW || C::kSepP, "the P V warp needs P in columns of its own");
+  // A negative scale arrives as a negative c2: the tensor core then computes
+  // S negated (Q negated as the A operand) and everything after S uses |c2|,
+  // so the row maximum and the masking below are those of a positive scale.
+  const uint32_t s_negate = c2 < 0.f ? kIdescNegateA : 0u;
+  c2 = fabsf(c2);
   static_assert(!F8 || (D == 128 && !DROP && !PVW), "FP8 Q, K: d = 128, no dropout, one issuer");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::threads(PVW), 1)
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer --
     {  // whole warp, converged: waits are warp-wide, one elected lane issues
-      constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0, 0);  // S = Q K^T, both K-major
+      const uint32_t idS = idesc_bf16(128, 128, 0, 0) | s_negate;  // S = (+/-) Q K^T, both K-major
       constexpr uint32_t kIdescO = idesc_bf16(128, D, 0, 1);    // O += P V, V is MN-major
       const uint32_t q_s = smem_addr(sm + C::kOffQ);
       const uint32_t k_s = smem_addr(sm + C::kOffK);
@@ -322,7 +327,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::threads(PVW), 1)
               mma_ss_f8_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024),
                           idesc_e4m3(128, 128), k > 0);
             else
-              mma_ss_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdescS,
+              mma_ss_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), idS,
                        k > 0);
           }
           mma_commit_w(&B.s_full[t]);

@@ -366,6 +366,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor bit that negates A (kind::f16): the product becomes
+// -(A B).  Used for S when the softmax scale is negative, so that everything
+// after S works with |scale|.
+constexpr uint32_t kIdescNegateA = 1u << 13;
+
 // Instruction descriptor, kind::f8f6f4: E4M3 A and B (format code 0 in both
 // type fields), fp32 accumulator, shape M x N, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {

@@ -23,8 +23,9 @@
  *           lse: contiguous [B, H, N] fp32.
  *  Sizes    B >= 1, H >= 1, N >= 1, d in {64, 128}; B*H*N*d < 2^31 elements
  *           per tensor; B*H < 2^31.
- *  scale    finite and >= 0 (typically 1/sqrt(d)); applied to Q K^T before
- *           the mask.
+ *  scale    any finite value (typically 1/sqrt(d); 0 gives uniform
+ *           attention, a negative value is allowed); applied to Q K^T
+ *           before the mask.
  *  causal   0: every key is visible.  1: key j is visible to query i iff
  *           j <= i (square, top-left aligned).  No other mask is supported.
  *  Pointers device pointers, 16-byte aligned; all memory is owned by the
@@ -91,12 +92,12 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  *   v         in   [B, H, N, d] bf16
  *   o, lse    out  as fa_fwd, for the scores scale * q_descale * k_descale *
  *                  (decoded Q)(decoded K)^T
- *   q_descale, k_descale  finite, >= 0
+ *   q_descale, k_descale  finite, >= 0 (and scale >= 0 here)
  *
  * One persistent kernel launch.  A NaN code makes the rows it reaches NaN.
  * Errors as fa_fwd, plus FA_ERR_UNSUPPORTED for d != 128 and
- * FA_ERR_INVALID_ARG for a negative or non-finite descale (or a non-finite
- * product with scale).
+ * FA_ERR_INVALID_ARG for a negative or non-finite descale, a negative scale,
+ * or a non-finite product of the three.
  */
 int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o, float* lse, int B, int H, int N, int d,
                float scale, float q_descale, float k_descale, int causal, cudaStream_t stream);

@@ -84,7 +84,6 @@ A = 1 << 20  # a 16-byte aligned fake address; validation fails before it is use
     (dict(causal=2), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
-    (dict(scale=-0.5), fa.FA_ERR_INVALID_ARG),
     (dict(q=None), fa.FA_ERR_INVALID_ARG),
     (dict(o=A + 8), fa.FA_ERR_INVALID_ARG),
     (dict(lse=A + 4), fa.FA_ERR_INVALID_ARG),
@@ -170,6 +169,7 @@ def test_dropout_rate_validation(lib, p):
     (dict(N=0), fa.FA_ERR_INVALID_ARG),
     (dict(causal=2), fa.FA_ERR_INVALID_ARG),
     (dict(q_descale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.125), fa.FA_ERR_INVALID_ARG),      # the E4M3 path takes no negative scale
     (dict(k_descale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(k_descale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(q_descale=3e38, k_descale=3e38), fa.FA_ERR_INVALID_ARG),   # product with scale overflows
@@ -238,7 +238,8 @@ BIG = dict(B=1, H=64, N=4096, d=128)
 
 @pytest.mark.parametrize("kw,code", [
     (dict(), fa.FA_ERR_WORKSPACE),                        # valid, too large: refused before any device work
-    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),            # bad arguments are named as such, whatever the size
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),    # bad arguments are named as such, whatever the size
+    (dict(scale=-1.0), fa.FA_ERR_WORKSPACE),              # a negative scale is valid
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(causal=2), fa.FA_ERR_INVALID_ARG),
     (dict(dq=A + 4), fa.FA_ERR_INVALID_ARG),

@@ -105,3 +105,13 @@ def test_workspace_rules():
     assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need, s) == fa.FA_OK
     assert fa.fa_fwd_splitkv_workspace_size(1, 2, 1, 1000, 64, 1) == 0   # one split: none needed
     assert fa.fa_get_device_status(s) == fa.FA_OK
+
+
+@pytest.mark.parametrize("Nq,Nk,d,splits", [(1, 2000, 128, 0), (4, 777, 64, 3)])
+def test_decode_negative_scale(Nq, Nk, d, splits):
+    scale = -1.0 / math.sqrt(d)
+    q, k, v = make_decode_inputs(1, 2, Nq, Nk, d, seed=5900 + Nq + Nk)
+    o, lse = _run(q, k, v, scale, True, splits)
+    o_ref, lse_ref = attention_forward_rect(*(t.double().numpy() for t in (q, k, v)), scale, True)
+    assert float(np.abs(f64(o) - o_ref).max()) <= TOL_O
+    assert float(np.abs(f64(lse) - lse_ref).max()) <= TOL_LSE

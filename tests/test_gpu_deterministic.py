@@ -63,3 +63,14 @@ def test_deterministic_full_workloads_sampled_heads(w):
         qd, kd, vd, dod = (sl(t).double().numpy() for t in (q, k, v, do))
         dq_r, dk_r, dv_r, _ = oracle.attention_backward(qd, kd, vd, dod, w.scale, w.causal)
         assert_grads_close((sl(dq), sl(dk), sl(dv)), (dq_r, dk_r, dv_r), f"{w.name} slice {(b, h)}")
+
+
+@pytest.mark.parametrize("d,causal", [(64, True), (128, False)])
+def test_deterministic_negative_scale(d, causal):
+    scale = -1.0 / math.sqrt(d)
+    q, k, v, do = make_inputs(1, 2, 400, d, seed=6500 + d)
+    qg, kg, vg, o, lse = run_fwd(q, k, v, scale, causal)
+    grads = _twice(qg, kg, vg, o, lse, do.cuda(), scale, causal)
+    qd, kd, vd, dod = (t.double().numpy() for t in (q, k, v, do))
+    dq_r, dk_r, dv_r, _ = oracle.attention_backward(qd, kd, vd, dod, scale, causal)
+    assert_grads_close(grads, (dq_r, dk_r, dv_r), f"deterministic scale<0 {(d, causal)}")

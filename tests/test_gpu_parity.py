@@ -126,3 +126,19 @@ def test_split_phases_match_oracle(B, H, N, d, causal):
         assert fa.fa_bwd_dq_convert(dq.data_ptr(), B, H, N, d, scale, ws.data_ptr(), nbytes, s) == fa.FA_OK
         assert fa.fa_get_device_status(s) == fa.FA_OK
         assert_grads_close((dq, dk, dv), g_ref, f"split {(B, H, N, d, causal)} rep {rep}")
+
+
+NEG = [(1, 2, 300, 64, False), (1, 2, 300, 64, True), (2, 1, 777, 128, False), (1, 2, 1000, 128, True),
+       (1, 1, 1100, 64, False), (1, 2, 4096, 128, True)]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", NEG, ids=[f"b{b}h{h}n{n}d{d}{'c' if c else ''}" for b, h, n, d, c in NEG])
+def test_negative_scale(B, H, N, d, causal):
+    """scale = -1/sqrt(d): the forward and backward match the oracle (S is formed negated on the tensor core)."""
+    scale = -1.0 / math.sqrt(d)
+    q, k, v, do = make_inputs(B, H, N, d, seed=7100 + N + d + causal)
+    qg, kg, vg, o, lse = run_fwd(q, k, v, scale, causal)
+    grads = run_bwd(qg, kg, vg, o, lse, do, scale, causal)
+    o_ref, lse_ref, g_ref = _oracle_case(q, k, v, do, scale, causal)
+    assert_fwd_close(o, lse, o_ref, lse_ref, f"scale<0 {(B, H, N, d, causal)}")
+    assert_grads_close(grads, g_ref, f"scale<0 {(B, H, N, d, causal)}")

@@ -204,3 +204,19 @@ def test_sampled_rows_equal_full_forward(causal):
     orow, lrow = attention_forward_head_rows(q[0, 0], k[0, 0], v[0, 0], rows, 0.25, causal)
     assert np.max(np.abs(orow - o[0, 0, rows])) < 1e-15
     assert np.max(np.abs(lrow - lse[0, 0, rows])) < 1e-15
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_negative_scale_matches_sdpa_and_negated_queries(causal):
+    """A negative scale is the positive one on negated queries; without a mask torch's SDPA agrees.
+
+    (torch's CPU SDPA returns NaN for a negative scale under its causal mask:
+    it masks before scaling, so a masked -inf times the scale becomes +inf.
+    The scale multiplies Q K^T before the mask here.)
+    """
+    q, k, v = (_rand((1, 2, 40, 8), s) for s in (51, 52, 53))
+    o1, lse1 = attention_forward(q, k, v, -0.3, causal)
+    o2, lse2 = attention_forward(-q, k, v, 0.3, causal)
+    assert np.max(np.abs(o1 - o2)) < 1e-13 and np.max(np.abs(lse1 - lse2)) < 1e-13
+    if not causal:
+        assert np.max(np.abs(o1 - _sdpa(q, k, v, -0.3, causal))) < 1e-12
