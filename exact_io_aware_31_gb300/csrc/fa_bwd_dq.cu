@@ -13,11 +13,16 @@
 // and at the end of the unit dQ = scale * dQ -> bf16.
 //
 // Roles (10 warps): two compute warpgroups (thread = query row, warpgroup g
-// owning key columns [64 g, 64 g + 64) of S and dP; its dS goes, packed as
-// bf16 pairs, over the first half of its own S columns), one TMA producer
-// warp (Q, dO and their lse2 / D rows per unit; K, V per key tile through a
-// ring), one MMA warp that owns the TMEM (S [0,128), dP [128,256),
-// dQ [256, 256 + d)).
+// owning keys [64 g, 64 g + 64) of every key tile: its S and dP columns, and
+// its dS packed as bf16 pairs over the first half of its own S columns), one
+// TMA producer warp (Q, dO and their lse2 / D rows per unit; K, V per key
+// tile through a ring), one MMA warp that owns the TMEM (S [0,128),
+// dP [128,256), dQ [256, 256 + d)).
+// The two key halves of a tile are separate MMAs with their own barriers, so
+// one warpgroup's dS overlaps the other half's MMAs.  Issue order:
+//     S_0 dP_0 | S_1 dP_1 | dQ += dS_0 K_0 | S_0 dP_0 (next tile) | dQ += dS_1 K_1 | S_1 dP_1 (next) ...
+// (each S_g of the next tile follows the dQ MMA that read dS_g from its
+// columns; the tensor pipe runs them in issue order).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -52,7 +57,7 @@ struct DqCfg {
   static constexpr int kOffRow = kOffV + kKvStages * kTileBytes;  // [q stages][-lse2 128 | -D 128] fp32
   static constexpr int kRowBytes = 2 * kTileRows * 4;
   static constexpr int kOffBar = kOffRow + kQStages * kRowBytes;
-  static constexpr int kNumBars = 2 * kQStages + 2 * kKvStages + 5;
+  static constexpr int kNumBars = 2 * kQStages + 2 * kKvStages + 7;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;
@@ -93,11 +98,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   uint64_t* q_empty = q_full + C::kQStages;        // [q stages]
   uint64_t* kv_full = q_empty + C::kQStages;       // [kv stages]
   uint64_t* kv_empty = kv_full + C::kKvStages;     // [kv stages]
-  uint64_t* s_full = kv_empty + C::kKvStages;      // S and dP of a key tile in TMEM
-  uint64_t* ds_full = s_full + 1;                  // dS of the tile in TMEM (compute threads)
-  uint64_t* dq_full = s_full + 2;                  // the unit's dQ complete
-  uint64_t* dq_empty = s_full + 3;                 // dQ read out (compute threads)
-  uint64_t* mma_done = s_full + 4;
+  uint64_t* s_full = kv_empty + C::kKvStages;      // [2] S and dP of key half g in TMEM
+  uint64_t* ds_full = s_full + 2;                  // [2] dS of key half g in TMEM (warpgroup g)
+  uint64_t* dq_full = s_full + 4;                  // the unit's dQ complete
+  uint64_t* dq_empty = s_full + 5;                 // dQ read out (compute threads)
+  uint64_t* mma_done = s_full + 6;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
 
@@ -118,8 +123,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(ds_full, C::kComputeThreads);
+    for (int g = 0; g < C::kWG; ++g) {
+      mbar_init(&s_full[g], 1);
+      mbar_init(&ds_full[g], 128);
+    }
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, C::kComputeThreads);
     mbar_init(mma_done, 1);
@@ -187,9 +194,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer --
     {  // whole warp, converged: waits are warp-wide, one elected lane issues
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // S, dP: A and B K-major over d
-      const uint32_t idS = kIdS | s_negate;                   // S = (+/-) Q K^T
-      constexpr uint32_t kIdQ = idesc_bf16(128, D, 0, 1);    // dQ += dS K: A from TMEM, B (K) MN-major
+      // S_g, dP_g: M = 128 queries, N = 64 keys of half g, A and B K-major over d
+      constexpr uint32_t kIdH = idesc_bf16(128, 64, 0, 0);
+      const uint32_t idS = kIdH | s_negate;                   // S_g = (+/-) Q K_g^T
+      constexpr uint32_t kIdQ = idesc_bf16(128, D, 0, 1);    // dQ += dS_g K_g: A from TMEM, B (K) MN-major
       auto kmajor = [](uint32_t base, int k) { return base + (k / 4) * kSwzBlockBytes + (k % 4) * 32; };
       uint32_t ucnt = 0, kvit = 0, dscnt = 0, dqcnt = 0;
       bool ok = true;
@@ -203,37 +211,63 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         const uint32_t q_s = smem_addr(sm + C::kOffQ + qs * C::kTileBytes);
         const uint32_t do_s = smem_addr(sm + C::kOffDO + qs * C::kTileBytes);
         if (!(ok = mbar_wait_warp(&q_full[qs], (ucnt / C::kQStages) & 1, status))) break;
+        // S_g and dP_g of key tile `it` (ring slot), keys [64 g, 64 g + 64): the
+        // B operand starts 64 rows (8 swizzle atoms, 8 KiB) into each block.
+        auto issue_half = [&](uint32_t it, int g) {
+          const int ks = it % C::kKvStages;
+          const uint32_t k_s = smem_addr(sm + C::kOffK + ks * C::kTileBytes) + 8192u * g;
+          const uint32_t v_s = smem_addr(sm + C::kOffV + ks * C::kTileBytes) + 8192u * g;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss_w(tbase + C::kColS + C::kKC * g, sdesc(kmajor(q_s, k), 16, 1024), sdesc(kmajor(k_s, k), 16, 1024),
+                     idS, k > 0);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss_w(tbase + C::kColDP + C::kKC * g, sdesc(kmajor(do_s, k), 16, 1024),
+                     sdesc(kmajor(v_s, k), 16, 1024), kIdH, k > 0);
+          mma_commit_w(&s_full[g]);
+        };
+        // dQ += dS_g K_g: A = dS_g (TMEM, over S_g), B = K rows [64 g, 64 g + 64)
+        auto issue_dq = [&](uint32_t it, int g, int j) {
+          const uint32_t k_s = smem_addr(sm + C::kOffK + (it % C::kKvStages) * C::kTileBytes);
+#pragma unroll
+          for (int k = 4 * g; k < 4 * g + 4; ++k)
+            mma_ts_w(tbase + C::kColDQ, tbase + C::kColS + dq_ds_col(k), sdesc(k_s + k * 2048, kSwzBlockBytes, 1024),
+                     kIdQ, (j > 0 || k > 0));
+        };
+        // prologue: both halves of the unit's first key tile
+        if (!(ok = mbar_wait_warp(&kv_full[kvit % C::kKvStages], (kvit / C::kKvStages) & 1, status))) break;
+        tc_fence_after();
+        issue_half(kvit, 0);
+        issue_half(kvit, 1);
         for (int j = 0; j < nkv && ok; ++j, ++kvit) {
-          const int ks = kvit % C::kKvStages;
-          const uint32_t k_s = smem_addr(sm + C::kOffK + ks * C::kTileBytes);
-          const uint32_t v_s = smem_addr(sm + C::kOffV + ks * C::kTileBytes);
-          if (!(ok = mbar_wait_warp(&kv_full[ks], (kvit / C::kKvStages) & 1, status))) break;
-          tc_fence_after();
-          // S = Q K^T and dP = dO V^T (their TMEM columns were last read by
-          // dQ of the previous key tile, issued before these)
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(tbase + C::kColS, sdesc(kmajor(q_s, k), 16, 1024), sdesc(kmajor(k_s, k), 16, 1024), idS, k > 0);
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(tbase + C::kColDP, sdesc(kmajor(do_s, k), 16, 1024), sdesc(kmajor(v_s, k), 16, 1024), kIdS,
-                   k > 0);
-          mma_commit_w(s_full);
-          // dQ += dS K_j, dS packed in TMEM over S
-          if (!(ok = mbar_wait_warp(ds_full, dscnt & 1, status))) break;
-          ++dscnt;
+          const bool more = j + 1 < nkv;
+          // half 0: its dS, then the next tile's S_0, dP_0 (over the dS just read)
+          if (!(ok = mbar_wait_warp(&ds_full[0], dscnt & 1, status))) break;
           // the first dQ MMA of a unit overwrites the columns: the previous
           // unit's dQ must have been read out
           if (j == 0 && !(ok = mbar_wait_warp(dq_empty, (dqcnt & 1) ^ 1, status))) break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ts_w(tbase + C::kColDQ, tbase + C::kColS + dq_ds_col(k),
-                   sdesc(k_s + k * 2048, kSwzBlockBytes, 1024), kIdQ, (j > 0 || k > 0));
-          mma_commit_w(&kv_empty[ks]);
+          issue_dq(kvit, 0, j);
+          if (more) {
+            if (!(ok = mbar_wait_warp(&kv_full[(kvit + 1) % C::kKvStages], ((kvit + 1) / C::kKvStages) & 1, status)))
+              break;
+            tc_fence_after();
+            issue_half(kvit + 1, 0);
+          }
+          // half 1
+          if (!(ok = mbar_wait_warp(&ds_full[1], dscnt & 1, status))) break;
+          ++dscnt;
+          tc_fence_after();
+          issue_dq(kvit, 1, j);
+          mma_commit_w(&kv_empty[kvit % C::kKvStages]);  // K_j, V_j have no later reader
+          if (more) issue_half(kvit + 1, 1);
+          // Q and dO have no later reader once the unit's last S_1, dP_1 are
+          // issued, and both warpgroups have read the unit's -lse2 / -D rows
+          // (before their first dS, waited for above): the slot may be reused.
+          if (j + 2 == nkv || nkv == 1) mma_commit_w(&q_empty[qs]);
         }
         if (!ok) break;
-        mma_commit_w(&q_empty[qs]);
         mma_commit_w(dq_full);
         ++dqcnt;
         ++ucnt;
@@ -268,7 +302,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       const uint64_t c2x2 = f2_pack(c2, c2);
       if (!(ok = mbar_wait_warp(&q_full[qs], (ucnt / C::kQStages) & 1, status))) break;  // the rows are in
       for (int j = 0; j < nkv; ++j) {
-        if (!(ok = mbar_wait_warp(s_full, scnt & 1, status))) break;
+        if (!(ok = mbar_wait_warp(&s_full[g], scnt & 1, status))) break;
         ++scnt;
         tc_fence_after();
         if (j == 0) {  // read before the unit's first dS is published (the copy slot is reused after)
@@ -309,7 +343,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         for (int c = 0; c < C::kKC / 32; ++c) tmem_st16(t_s + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(ds_full);
+        mbar_arrive(&ds_full[g]);
       }
       if (!ok) break;
       // ---- epilogue: this warpgroup's half of the dQ columns -> scale * dQ, bf16 ----

@@ -8,7 +8,7 @@
 // streams K/V tiles past them, writing O once).
 //
 // Work unit: 256 query rows (two 128-row Q tiles, t = 0, 1) of one (b, h).
-// CTA roles (10 warps; 11 with PVW):
+// CTA roles (12 warps; warps 10-11 idle without PVW, warp 11 idle with it):
 //   warps 0-3  softmax warpgroup for Q tile 0   (thread = one query row)
 //   warps 4-7  softmax warpgroup for Q tile 1
 //   warp  8    TMA producer: Q tiles, then K_j / V_j into a STAGES-deep ring
@@ -82,7 +82,17 @@ struct FwdCfg {
   static constexpr int kColP = kSepP ? 256 : 0;     // + kPStride t
   static constexpr int kPStride = kSepP ? 64 : 128;
   static constexpr int kColO = kSepP ? 384 : 256;   // + D t
-  static constexpr int threads(bool pvw) { return pvw ? 352 : 320; }
+  // 12 warps: two softmax warpgroups and one of producer, MMA issuer(s) and
+  // idle warps.  Launched at 168 registers a thread (three warps on each SM
+  // sub-partition, one of each warpgroup); the third warpgroup gives
+  // registers back so the softmax threads can hold a whole score row (and
+  // its exponentials) without spilling: 2 x 128 x kSoftmaxRegs + 128 x
+  // kAuxRegs = 384 x 168, which also balances on every sub-partition.
+  static constexpr int kThreads = 384;
+  static constexpr int kLaunchRegs = 168;
+  static constexpr int kAuxRegs = 104;      // the MMA issuer's loop needs about 100
+  static constexpr int kSoftmaxRegs = 200;  // no spills at d = 64 or 128 (dropout aside)
+  static_assert(2 * 128 * kSoftmaxRegs + 128 * kAuxRegs <= kThreads * kLaunchRegs, "register split");
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQBufs * kQKBytes;
@@ -149,7 +159,7 @@ __device__ __forceinline__ FwdUnit fwd_decode(int pos, int BH, int nqb, int N, i
 // every probability, the P fed to P V keeps only the surviving ones, and the
 // epilogue scales O by 1 / (1 - p).
 template <int D, bool CAUSAL, bool DROP, bool PVW, bool F8 = false>
-__global__ void __launch_bounds__(FwdCfg<D, F8>::threads(PVW), 1)
+__global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ lse, int BH, int N, float c2, DropParams dp, int* status) {
@@ -220,185 +230,221 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::threads(PVW), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      Tracer tr(3);
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_k);
-      tma_prefetch_map(&tm_v);
-      uint32_t qcnt[2] = {0, 0};
-      uint32_t kv_it = 0;
-      bool ok = true;
-      for (int round = 0; ok; ++round) {
-        const int pos = snake_unit(round, blockIdx.x, grid);
-        if (round * grid >= total_units) break;
-        if (pos >= total_units) continue;
-        const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
-        tr(30);
-        #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t >= u.nq || !ok) continue;
-          const int qb = t * C::kQBufs + qcnt[t] % C::kQBufs;
-          ok = mbar_wait(&B.q_empty[qb], ((qcnt[t] / C::kQBufs) & 1) ^ 1, status);
-          tr(31);
-          if (!ok) break;
-          uint8_t* dst = sm + C::kOffQ + qb * C::kQKBytes;
-          mbar_expect_tx(&B.q_full[qb], C::kQKBytes);
-          for (int kb = 0; kb < C::kQKBlocks; ++kb)
-            tma_load_3d(dst + kb * kSwzBlockBytes, &tm_q, &B.q_full[qb], kb * C::kQKBlockCols, u.q0 + t * kTileRows,
-                        u.bh);
-          ++qcnt[t];
-        }
-        for (int j = 0; j < u.nkv_max && ok; ++j, ++kv_it) {
-          const int st = kv_it % C::kStages;
-          const uint32_t ph = (kv_it / C::kStages) & 1;
-          tr(32);
-          ok = mbar_wait(&B.kv_empty[st], ph ^ 1, status);
-          tr(33);
-          if (!ok) break;
-          uint8_t* kd = sm + C::kOffK + st * C::kQKBytes;
-          uint8_t* vd = sm + C::kOffV + st * C::kTileBytes;
-          mbar_expect_tx(&B.k_full[st], C::kQKBytes);
-          for (int kb = 0; kb < C::kQKBlocks; ++kb)
-            tma_load_3d(kd + kb * kSwzBlockBytes, &tm_k, &B.k_full[st], kb * C::kQKBlockCols, j * kTileRows, u.bh);
-          if (PVW && !(ok = mbar_wait(&B.v_empty[st], ph ^ 1, status))) break;
-          mbar_expect_tx(&B.v_full[st], C::kTileBytes);
-          for (int kb = 0; kb < C::kBlocks; ++kb)
-            tma_load_3d(vd + kb * kSwzBlockBytes, &tm_v, &B.v_full[st], kb * 64, j * kTileRows, u.bh);
-        }
-        if (aborted(abort_flag)) ok = false;
-      }
-      if (!ok) {
-        *abort_flag = 1;
-      }
-      // Drain: every copy this warp started must have landed before exit.
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-        for (uint32_t x = (qcnt[t] > (uint32_t)C::kQBufs ? qcnt[t] - C::kQBufs : 0); x < qcnt[t]; ++x)
-          mbar_wait(&B.q_full[t * C::kQBufs + x % C::kQBufs], (x / C::kQBufs) & 1, status);
-      for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i) {
-        mbar_wait(&B.k_full[i % C::kStages], (i / C::kStages) & 1, status);
-        mbar_wait(&B.v_full[i % C::kStages], (i / C::kStages) & 1, status);
-      }
-    }
-  } else if (warp == 9) {
-    // ---------------------------------------------------------- MMA issuer --
-    {  // whole warp, converged: waits are warp-wide, one elected lane issues
-      const uint32_t idS = idesc_bf16(128, 128, 0, 0) | s_negate;  // S = (+/-) Q K^T, both K-major
-      constexpr uint32_t kIdescO = idesc_bf16(128, D, 0, 1);    // O += P V, V is MN-major
-      const uint32_t q_s = smem_addr(sm + C::kOffQ);
-      const uint32_t k_s = smem_addr(sm + C::kOffK);
-      const uint32_t v_s = smem_addr(sm + C::kOffV);
-      uint32_t qcnt[2] = {0, 0}, pcnt[2] = {0, 0};
-      uint32_t sis[2] = {0, 0};  // S_t issued so far (kSepP: each after the softmax read the previous one)
-      uint32_t kv_it = 0;
-      bool ok = true;
-      Tracer tr(2);
-      for (int round = 0; ok; ++round) {
-        const int pos = snake_unit(round, blockIdx.x, grid);
-        if (round * grid >= total_units) break;
-        if (pos >= total_units) continue;
-        const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
-        tr(10);
-        int qbuf[2] = {0, 0};  // Q buffer (t * kQBufs + b) each tile uses in this unit
-        #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t >= u.nq || !ok) continue;
-          qbuf[t] = t * C::kQBufs + qcnt[t] % C::kQBufs;
-          ok = mbar_wait_warp(&B.q_full[qbuf[t]], (qcnt[t] / C::kQBufs) & 1, status);
-          ++qcnt[t];
-        }
-        tr(11);
-        if (!ok) break;
-        auto issue_s = [&](int t, int st) -> bool {
-          if (C::kSepP) {  // S_t columns are free once the softmax has read the previous S_t
-            if (sis[t] > 0 && !mbar_wait_warp(&B.s_free[t], (sis[t] - 1) & 1, status)) return false;
-            tc_fence_after();
-          }
-          ++sis[t];
-          const uint32_t qa = q_s + qbuf[t] * C::kQKBytes, ka = k_s + st * C::kQKBytes;
-          // 32 bytes of the 128-byte swizzled rows a step: 16 bf16 or 32 E4M3 elements
-#pragma unroll
-          for (int k = 0; k < D / (F8 ? 32 : 16); ++k) {
-            const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
-            if constexpr (F8)
-              mma_ss_f8_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024),
-                          idesc_e4m3(128, 128), k > 0);
-            else
-              mma_ss_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), idS,
-                       k > 0);
-          }
-          mma_commit_w(&B.s_full[t]);
-          return true;
-        };
-        // prologue: S_t(0)
-        {
-          const int st = kv_it % C::kStages;
-          ok = mbar_wait_warp(&B.k_full[st], (kv_it / C::kStages) & 1, status);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
+  // Each role's code starts with its warpgroup's register budget: warps 8-11
+  // (producer, MMA issuer(s), idle) give registers back, the softmax
+  // warpgroups take them.
+  if (warp >= 8) {
+    regs_dec<C::kAuxRegs>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ producer --
+      if (lane == 0) {
+        Tracer tr(3);
+        tma_prefetch_map(&tm_q);
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+        uint32_t qcnt[2] = {0, 0};
+        uint32_t kv_it = 0;
+        bool ok = true;
+        for (int round = 0; ok; ++round) {
+          const int pos = snake_unit(round, blockIdx.x, grid);
+          if (round * grid >= total_units) break;
+          if (pos >= total_units) continue;
+          const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
+          tr(30);
+          #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (t < u.nq && ok) ok = issue_s(t, st);
-            if (t < u.nq && ok && u.nkv(t) == 1) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+            if (t >= u.nq || !ok) continue;
+            const int qb = t * C::kQBufs + qcnt[t] % C::kQBufs;
+            ok = mbar_wait(&B.q_empty[qb], ((qcnt[t] / C::kQBufs) & 1) ^ 1, status);
+            tr(31);
+            if (!ok) break;
+            uint8_t* dst = sm + C::kOffQ + qb * C::kQKBytes;
+            mbar_expect_tx(&B.q_full[qb], C::kQKBytes);
+            for (int kb = 0; kb < C::kQKBlocks; ++kb)
+              tma_load_3d(dst + kb * kSwzBlockBytes, &tm_q, &B.q_full[qb], kb * C::kQKBlockCols, u.q0 + t * kTileRows,
+                          u.bh);
+            ++qcnt[t];
           }
-          if (!ok) break;
+          for (int j = 0; j < u.nkv_max && ok; ++j, ++kv_it) {
+            const int st = kv_it % C::kStages;
+            const uint32_t ph = (kv_it / C::kStages) & 1;
+            tr(32);
+            ok = mbar_wait(&B.kv_empty[st], ph ^ 1, status);
+            tr(33);
+            if (!ok) break;
+            uint8_t* kd = sm + C::kOffK + st * C::kQKBytes;
+            uint8_t* vd = sm + C::kOffV + st * C::kTileBytes;
+            mbar_expect_tx(&B.k_full[st], C::kQKBytes);
+            for (int kb = 0; kb < C::kQKBlocks; ++kb)
+              tma_load_3d(kd + kb * kSwzBlockBytes, &tm_k, &B.k_full[st], kb * C::kQKBlockCols, j * kTileRows, u.bh);
+            if (PVW && !(ok = mbar_wait(&B.v_empty[st], ph ^ 1, status))) break;
+            mbar_expect_tx(&B.v_full[st], C::kTileBytes);
+            for (int kb = 0; kb < C::kBlocks; ++kb)
+              tma_load_3d(vd + kb * kSwzBlockBytes, &tm_v, &B.v_full[st], kb * 64, j * kTileRows, u.bh);
+          }
+          if (aborted(abort_flag)) ok = false;
         }
-        if constexpr (PVW) {
-          // Per key tile j: S_0(j+1), S_1(j+1), each once the softmax has read
-          // S_t(j); then K_j is released (its S MMAs were issued before).
-          for (int j = 0; j < u.nkv_max && ok; ++j) {
-            const uint32_t it = kv_it + j;
-            const int st = it % C::kStages;
-            const int st_next = (it + 1) % C::kStages;
-            bool k_next_ready = false;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (t >= u.nq || j + 1 >= u.nkv(t) || !ok) continue;
-              if (!k_next_ready) {
-                ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                k_next_ready = true;
-              }
-              tr(40 + t);
-              ok = issue_s(t, st_next);
-              if (!ok) break;
-              if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
-              tr(24 + t);
-            }
-            if (ok) mma_commit_w(&B.kv_empty[st]);
+        if (!ok) {
+          *abort_flag = 1;
+        }
+        // Drain: every copy this warp started must have landed before exit.
+  #pragma unroll
+        for (int t = 0; t < 2; ++t)
+          for (uint32_t x = (qcnt[t] > (uint32_t)C::kQBufs ? qcnt[t] - C::kQBufs : 0); x < qcnt[t]; ++x)
+            mbar_wait(&B.q_full[t * C::kQBufs + x % C::kQBufs], (x / C::kQBufs) & 1, status);
+        for (uint32_t i = (kv_it > (uint32_t)C::kStages ? kv_it - C::kStages : 0); i < kv_it; ++i) {
+          mbar_wait(&B.k_full[i % C::kStages], (i / C::kStages) & 1, status);
+          mbar_wait(&B.v_full[i % C::kStages], (i / C::kStages) & 1, status);
+        }
+      }
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer --
+      {  // whole warp, converged: waits are warp-wide, one elected lane issues
+        const uint32_t idS = idesc_bf16(128, 128, 0, 0) | s_negate;  // S = (+/-) Q K^T, both K-major
+        constexpr uint32_t kIdescO = idesc_bf16(128, D, 0, 1);    // O += P V, V is MN-major
+        const uint32_t q_s = smem_addr(sm + C::kOffQ);
+        const uint32_t k_s = smem_addr(sm + C::kOffK);
+        const uint32_t v_s = smem_addr(sm + C::kOffV);
+        uint32_t qcnt[2] = {0, 0}, pcnt[2] = {0, 0};
+        uint32_t sis[2] = {0, 0};  // S_t issued so far (kSepP: each after the softmax read the previous one)
+        uint32_t kv_it = 0;
+        bool ok = true;
+        Tracer tr(2);
+        for (int round = 0; ok; ++round) {
+          const int pos = snake_unit(round, blockIdx.x, grid);
+          if (round * grid >= total_units) break;
+          if (pos >= total_units) continue;
+          const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
+          tr(10);
+          int qbuf[2] = {0, 0};  // Q buffer (t * kQBufs + b) each tile uses in this unit
+          #pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t >= u.nq || !ok) continue;
+            qbuf[t] = t * C::kQBufs + qcnt[t] % C::kQBufs;
+            ok = mbar_wait_warp(&B.q_full[qbuf[t]], (qcnt[t] / C::kQBufs) & 1, status);
+            ++qcnt[t];
           }
-        } else if constexpr (C::kSepP) {
-          // Per key tile j: S_0(j+1), S_1(j+1) (each once the softmax has read
-          // S_t(j)), then P_t V_j for each tile once P_t(j) is written.
-          for (int j = 0; j < u.nkv_max && ok; ++j) {
-            const uint32_t it = kv_it + j;
-            const int st = it % C::kStages;
-            const int st_next = (it + 1) % C::kStages;
-            bool k_next_ready = false;
-#pragma unroll
+          tr(11);
+          if (!ok) break;
+          auto issue_s = [&](int t, int st) -> bool {
+            if (C::kSepP) {  // S_t columns are free once the softmax has read the previous S_t
+              if (sis[t] > 0 && !mbar_wait_warp(&B.s_free[t], (sis[t] - 1) & 1, status)) return false;
+              tc_fence_after();
+            }
+            ++sis[t];
+            const uint32_t qa = q_s + qbuf[t] * C::kQKBytes, ka = k_s + st * C::kQKBytes;
+            // 32 bytes of the 128-byte swizzled rows a step: 16 bf16 or 32 E4M3 elements
+  #pragma unroll
+            for (int k = 0; k < D / (F8 ? 32 : 16); ++k) {
+              const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
+              if constexpr (F8)
+                mma_ss_f8_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024),
+                            idesc_e4m3(128, 128), k > 0);
+              else
+                mma_ss_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), idS,
+                         k > 0);
+            }
+            mma_commit_w(&B.s_full[t]);
+            return true;
+          };
+          // prologue: S_t(0)
+          {
+            const int st = kv_it % C::kStages;
+            ok = mbar_wait_warp(&B.k_full[st], (kv_it / C::kStages) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+  #pragma unroll
             for (int t = 0; t < 2; ++t) {
-              if (t >= u.nq || j + 1 >= u.nkv(t) || !ok) continue;
-              if (!k_next_ready) {
-                ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                k_next_ready = true;
-              }
-              tr(40 + t);
-              ok = issue_s(t, st_next);
-              if (!ok) break;
-              if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
-              tr(24 + t);
+              if (t < u.nq && ok) ok = issue_s(t, st);
+              if (t < u.nq && ok && u.nkv(t) == 1) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
             }
             if (!ok) break;
-            bool v_ready = false;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (t >= u.nq || j >= u.nkv(t) || !ok) continue;
+          }
+          if constexpr (PVW) {
+            // Per key tile j: S_0(j+1), S_1(j+1), each once the softmax has read
+            // S_t(j); then K_j is released (its S MMAs were issued before).
+            for (int j = 0; j < u.nkv_max && ok; ++j) {
+              const uint32_t it = kv_it + j;
+              const int st = it % C::kStages;
+              const int st_next = (it + 1) % C::kStages;
+              bool k_next_ready = false;
+  #pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (t >= u.nq || j + 1 >= u.nkv(t) || !ok) continue;
+                if (!k_next_ready) {
+                  ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
+                  if (!ok) break;
+                  tc_fence_after();
+                  k_next_ready = true;
+                }
+                tr(40 + t);
+                ok = issue_s(t, st_next);
+                if (!ok) break;
+                if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+                tr(24 + t);
+              }
+              if (ok) mma_commit_w(&B.kv_empty[st]);
+            }
+          } else if constexpr (C::kSepP) {
+            // Per key tile j: S_0(j+1), S_1(j+1) (each once the softmax has read
+            // S_t(j)), then P_t V_j for each tile once P_t(j) is written.
+            for (int j = 0; j < u.nkv_max && ok; ++j) {
+              const uint32_t it = kv_it + j;
+              const int st = it % C::kStages;
+              const int st_next = (it + 1) % C::kStages;
+              bool k_next_ready = false;
+  #pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (t >= u.nq || j + 1 >= u.nkv(t) || !ok) continue;
+                if (!k_next_ready) {
+                  ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
+                  if (!ok) break;
+                  tc_fence_after();
+                  k_next_ready = true;
+                }
+                tr(40 + t);
+                ok = issue_s(t, st_next);
+                if (!ok) break;
+                if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+                tr(24 + t);
+              }
+              if (!ok) break;
+              bool v_ready = false;
+  #pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (t >= u.nq || j >= u.nkv(t) || !ok) continue;
+                tr(20 + t);
+                ok = mbar_wait_warp(&B.p_full[t], pcnt[t] & 1, status);
+                tr(22 + t);
+                ++pcnt[t];
+                if (!ok) break;
+                if (!v_ready) {
+                  ok = mbar_wait_warp(&B.v_full[st], (it / C::kStages) & 1, status);
+                  if (!ok) break;
+                  v_ready = true;
+                }
+                tr(26 + t);
+                tc_fence_after();
+                const uint32_t va = v_s + st * C::kTileBytes;
+  #pragma unroll
+                for (int k = 0; k < kTileRows / 16; ++k)
+                  mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t + k * 8,
+                           sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
+                mma_commit_w(&B.pv_done[t]);
+                tr(28 + t);
+              }
+              if (ok) mma_commit_w(&B.kv_empty[st]);
+            }
+          } else
+          for (int j = 0; j < u.nkv_max && ok; ++j) {
+            const uint32_t it = kv_it + j;
+            const int st = it % C::kStages;
+            const int st_next = (it + 1) % C::kStages;
+            bool v_ready = false, k_next_ready = false;
+            #pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t >= u.nq || !ok) continue;
+              if (j >= u.nkv(t)) continue;
               tr(20 + t);
               ok = mbar_wait_warp(&B.p_full[t], pcnt[t] & 1, status);
               tr(22 + t);
@@ -411,117 +457,87 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::threads(PVW), 1)
               }
               tr(26 + t);
               tc_fence_after();
+              // O_t (+)= P_t V_j : A = P_t from TMEM (8 columns per 16 keys), B = V_j MN-major
               const uint32_t va = v_s + st * C::kTileBytes;
-#pragma unroll
+  #pragma unroll
+              for (int k = 0; k < kTileRows / 16; ++k)
+                mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColS + 128 * t + k * 8,
+                       sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
+              tr(28 + t);
+              if (j + 1 < u.nkv(t)) {
+                if (!k_next_ready) {
+                  ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
+                  if (!ok) break;
+                  tc_fence_after();
+                  k_next_ready = true;
+                }
+                tr(40 + t);
+                ok = issue_s(t, st_next);
+                if (!ok) break;
+                if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
+              } else {
+                mma_commit_w(&B.o_full[t]);
+              }
+              tr(24 + t);
+            }
+            if (ok) mma_commit_w(&B.kv_empty[st]);
+          }
+          kv_it += u.nkv_max;
+          if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
+        }
+        if (!ok) *abort_flag = 1;
+        mma_commit_w(B.mma_done);
+        mbar_wait_warp(B.mma_done, 0, status);
+      }
+    } else if (PVW && warp == 10) {
+      // ------------------------------------------------------ P V issuer (PVW) --
+      {  // whole warp, converged: waits are warp-wide, one elected lane issues
+        constexpr uint32_t kIdescO = idesc_bf16(128, D, 0, 1);  // O += P V, V is MN-major
+        const uint32_t v_s = smem_addr(sm + C::kOffV);
+        uint32_t pcnt[2] = {0, 0};
+        uint32_t kv_it = 0;
+        bool ok = true;
+        for (int round = 0; ok; ++round) {
+          const int pos = snake_unit(round, blockIdx.x, grid);
+          if (round * grid >= total_units) break;
+          if (pos >= total_units) continue;
+          const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
+          for (int j = 0; j < u.nkv_max && ok; ++j) {
+            const uint32_t it = kv_it + j;
+            const int st = it % C::kStages;
+            bool v_ready = false;
+  #pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (t >= u.nq || j >= u.nkv(t) || !ok) continue;
+              ok = mbar_wait_warp(&B.p_full[t], pcnt[t] & 1, status);
+              ++pcnt[t];
+              if (!ok) break;
+              if (!v_ready) {
+                ok = mbar_wait_warp(&B.v_full[st], (it / C::kStages) & 1, status);
+                if (!ok) break;
+                v_ready = true;
+              }
+              tc_fence_after();
+              // O_t (+)= P_t V_j : A = P_t from TMEM (8 columns per 16 keys), B = V_j MN-major
+              const uint32_t va = v_s + st * C::kTileBytes;
+  #pragma unroll
               for (int k = 0; k < kTileRows / 16; ++k)
                 mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t + k * 8,
                          sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
               mma_commit_w(&B.pv_done[t]);
-              tr(28 + t);
             }
-            if (ok) mma_commit_w(&B.kv_empty[st]);
+            if (ok) mma_commit_w(&B.v_empty[st]);
           }
-        } else
-        for (int j = 0; j < u.nkv_max && ok; ++j) {
-          const uint32_t it = kv_it + j;
-          const int st = it % C::kStages;
-          const int st_next = (it + 1) % C::kStages;
-          bool v_ready = false, k_next_ready = false;
-          #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t >= u.nq || !ok) continue;
-            if (j >= u.nkv(t)) continue;
-            tr(20 + t);
-            ok = mbar_wait_warp(&B.p_full[t], pcnt[t] & 1, status);
-            tr(22 + t);
-            ++pcnt[t];
-            if (!ok) break;
-            if (!v_ready) {
-              ok = mbar_wait_warp(&B.v_full[st], (it / C::kStages) & 1, status);
-              if (!ok) break;
-              v_ready = true;
-            }
-            tr(26 + t);
-            tc_fence_after();
-            // O_t (+)= P_t V_j : A = P_t from TMEM (8 columns per 16 keys), B = V_j MN-major
-            const uint32_t va = v_s + st * C::kTileBytes;
-#pragma unroll
-            for (int k = 0; k < kTileRows / 16; ++k)
-              mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColS + 128 * t + k * 8,
-                     sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
-            tr(28 + t);
-            if (j + 1 < u.nkv(t)) {
-              if (!k_next_ready) {
-                ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                k_next_ready = true;
-              }
-              tr(40 + t);
-              ok = issue_s(t, st_next);
-              if (!ok) break;
-              if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
-            } else {
-              mma_commit_w(&B.o_full[t]);
-            }
-            tr(24 + t);
-          }
-          if (ok) mma_commit_w(&B.kv_empty[st]);
+          kv_it += u.nkv_max;
+          if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
         }
-        kv_it += u.nkv_max;
-        if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
+        if (!ok) *abort_flag = 1;
+        mma_commit_w(B.mma_done);
+        mbar_wait_warp(B.mma_done, 0, status);
       }
-      if (!ok) *abort_flag = 1;
-      mma_commit_w(B.mma_done);
-      mbar_wait_warp(B.mma_done, 0, status);
-    }
-  } else if (PVW && warp == 10) {
-    // ------------------------------------------------------ P V issuer (PVW) --
-    {  // whole warp, converged: waits are warp-wide, one elected lane issues
-      constexpr uint32_t kIdescO = idesc_bf16(128, D, 0, 1);  // O += P V, V is MN-major
-      const uint32_t v_s = smem_addr(sm + C::kOffV);
-      uint32_t pcnt[2] = {0, 0};
-      uint32_t kv_it = 0;
-      bool ok = true;
-      for (int round = 0; ok; ++round) {
-        const int pos = snake_unit(round, blockIdx.x, grid);
-        if (round * grid >= total_units) break;
-        if (pos >= total_units) continue;
-        const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
-        for (int j = 0; j < u.nkv_max && ok; ++j) {
-          const uint32_t it = kv_it + j;
-          const int st = it % C::kStages;
-          bool v_ready = false;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (t >= u.nq || j >= u.nkv(t) || !ok) continue;
-            ok = mbar_wait_warp(&B.p_full[t], pcnt[t] & 1, status);
-            ++pcnt[t];
-            if (!ok) break;
-            if (!v_ready) {
-              ok = mbar_wait_warp(&B.v_full[st], (it / C::kStages) & 1, status);
-              if (!ok) break;
-              v_ready = true;
-            }
-            tc_fence_after();
-            // O_t (+)= P_t V_j : A = P_t from TMEM (8 columns per 16 keys), B = V_j MN-major
-            const uint32_t va = v_s + st * C::kTileBytes;
-#pragma unroll
-            for (int k = 0; k < kTileRows / 16; ++k)
-              mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t + k * 8,
-                       sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
-            mma_commit_w(&B.pv_done[t]);
-          }
-          if (ok) mma_commit_w(&B.v_empty[st]);
-        }
-        kv_it += u.nkv_max;
-        if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
-      }
-      if (!ok) *abort_flag = 1;
-      mma_commit_w(B.mma_done);
-      mbar_wait_warp(B.mma_done, 0, status);
     }
   } else {
+    regs_inc<C::kSoftmaxRegs>();
     // -------------------------------------------------------------- softmax --
     const int t = warp / 4;            // which Q tile this warpgroup owns
     const int quarter = warp % 4;      // TMEM lane quarter
@@ -714,9 +730,17 @@ template <int D, bool CAUSAL, bool DROP, bool PVW = false, bool F8 = false>
 static cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   using C = FwdCfg<D, F8>;
   auto kern = fa_fwd_kernel<D, CAUSAL, DROP, PVW, F8>;
+  // The register split inside the kernel assumes it was built with exactly
+  // kLaunchRegs registers a thread: with fewer, the softmax warpgroups' request
+  // for more could never be met.  Refuse to launch such a build.
+  static const bool regs_ok = [&] {
+    cudaFuncAttributes fa_attr;
+    return cudaFuncGetAttributes(&fa_attr, kern) == cudaSuccess && fa_attr.numRegs == C::kLaunchRegs;
+  }();
+  if (!regs_ok) return cudaErrorInvalidKernelImage;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, C::threads(PVW), C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v,
+  kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v,
                                                        reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.N,
                                                        a.c2, a.drop, a.status);
   return cudaGetLastError();

@@ -128,6 +128,22 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, i
   }
 }
 
+// ------------------------------------------------------ register budgets ----
+// Move this warpgroup's per-thread register budget up or down (all four warps
+// of the warpgroup execute it).  The registers a warpgroup gives back go to
+// the others of the block; the block's total is what it was launched with, so
+// the budgets a kernel sets must add up to no more than that total.
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register budget");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register budget");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ fences --
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -9,8 +9,10 @@ P rounded to bf16 before P V under the lazy running maximum, the output
 rounded to bf16, and in the backward bf16 P, bf16 dS and D from that stored
 output):
 
-* O: at most two bf16 units in the last place from the model's stored O,
-  and bit-identical in most elements;
+* O: within two bf16 units in the last place of the model's stored O (or
+  1e-3 where O is small enough for that to be more), and bit-identical in
+  most elements: one rounding on each side plus the odd probability that
+  fp32 and fp64 round to neighbouring bf16 values;
 * lse: the plain 1e-3;
 * dQ, dK, dV: the plain 2e-2 of each gradient's max-abs, with no allowance.
 """
@@ -36,11 +38,10 @@ def _gpu():
     require_gpu()
 
 
-def _ulps(a, b):
-    """|a - b| in units of the last place of bf16 at b (b a bf16 value)."""
+def _bf16_ulp(b):
+    """The spacing of bf16 values at b (8 significant bits)."""
     _, e = np.frexp(b)
-    ulp = np.ldexp(1.0, np.maximum(e, -125) - 8)
-    return np.abs(a - b) / ulp
+    return np.ldexp(1.0, np.maximum(e, -125) - 8)
 
 
 @pytest.mark.parametrize("stress,N,d,causal", STRESS, ids=[f"{s}-n{n}d{d}{'c' if c else ''}" for s, n, d, c in STRESS])
@@ -54,13 +55,13 @@ def test_stress_residual_is_bf16_rounding(stress, N, d, causal):
     for h in range(2):
         qd, kd, vd, dod = (t[0, h].double().numpy() for t in (q, k, v, do))
         _, o_b, lse_m = attention_forward_bf16(qd, kd, vd, scale, causal)
-        u = _ulps(o_g[0, h], o_b)
-        worst = max(worst, float(u.max()))
-        identical += int((u == 0).sum())
+        diff = np.abs(o_g[0, h] - o_b)
+        worst = max(worst, float((diff - np.maximum(2.0 * _bf16_ulp(o_b), 1e-3)).max()))
+        identical += int((diff == 0).sum())
         assert float(np.abs(lse_g[0, h] - lse_m).max()) <= TOL_LSE
         grads = attention_backward_bf16(qd, kd, vd, dod, scale, causal, o_b, lse_m)
         for name, g, r in zip(("dq", "dk", "dv"), (dq[0, h], dk[0, h], dv[0, h]), grads):
             err = float(np.abs(f64(g) - r).max())
             assert err <= TOL_GRAD_REL * float(np.abs(r).max()), f"{stress} head {h} {name}: {err}"
-    assert worst <= 2.0, f"{stress}: O is {worst} bf16 ulps from the model"
+    assert worst <= 0.0, f"{stress}: O beyond two bf16 ulps (and 1e-3) of the model by {worst}"
     assert identical >= 0.8 * o_g.size, f"{stress}: only {identical} of {o_g.size} O elements equal the model's"
