@@ -201,12 +201,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       auto kmajor = [](uint32_t base, int k) { return base + (k / 4) * kSwzBlockBytes + (k % 4) * 32; };
       uint32_t ucnt = 0, kvit = 0, dscnt = 0, dqcnt = 0;
       bool ok = true;
+      Tracer tr(2);
       for (int round = 0; ok; ++round) {
         if (round * grid >= total_units) break;
         const int pos = snake_unit(round, blockIdx.x, grid);
         if (pos >= total_units) continue;
         int bh, i, nkv;
         dq_decode(pos, BH, nqt, CAUSAL, block_major, bh, i, nkv);
+        tr(10);
         const int qs = ucnt % C::kQStages;
         const uint32_t q_s = smem_addr(sm + C::kOffQ + qs * C::kTileBytes);
         const uint32_t do_s = smem_addr(sm + C::kOffDO + qs * C::kTileBytes);
@@ -243,7 +245,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         for (int j = 0; j < nkv && ok; ++j, ++kvit) {
           const bool more = j + 1 < nkv;
           // half 0: its dS, then the next tile's S_0, dP_0 (over the dS just read)
+          tr(20);
           if (!(ok = mbar_wait_warp(&ds_full[0], dscnt & 1, status))) break;
+          tr(21);
           // the first dQ MMA of a unit overwrites the columns: the previous
           // unit's dQ must have been read out
           if (j == 0 && !(ok = mbar_wait_warp(dq_empty, (dqcnt & 1) ^ 1, status))) break;
@@ -256,12 +260,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             issue_half(kvit + 1, 0);
           }
           // half 1
+          tr(22);
           if (!(ok = mbar_wait_warp(&ds_full[1], dscnt & 1, status))) break;
+          tr(23);
           ++dscnt;
           tc_fence_after();
           issue_dq(kvit, 1, j);
           mma_commit_w(&kv_empty[kvit % C::kKvStages]);  // K_j, V_j have no later reader
           if (more) issue_half(kvit + 1, 1);
+          tr(24);
           // Q and dO have no later reader once the unit's last S_1, dP_1 are
           // issued, and both warpgroups have read the unit's -lse2 / -D rows
           // (before their first dS, waited for above): the slot may be reused.
@@ -288,6 +295,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + (D / 2) * g);
     uint32_t ucnt = 0, scnt = 0, dqcnt = 0;
     bool ok = true;
+    Tracer tr((warp % 4) == 0 ? g : -1);
     for (int round = 0; ok; ++round) {
       if (round * grid >= total_units) break;
       const int pos = snake_unit(round, blockIdx.x, grid);
@@ -302,7 +310,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       const uint64_t c2x2 = f2_pack(c2, c2);
       if (!(ok = mbar_wait_warp(&q_full[qs], (ucnt / C::kQStages) & 1, status))) break;  // the rows are in
       for (int j = 0; j < nkv; ++j) {
+        tr(1);
         if (!(ok = mbar_wait_warp(&s_full[g], scnt & 1, status))) break;
+        tr(2);
         ++scnt;
         tc_fence_after();
         if (j == 0) {  // read before the unit's first dS is published (the copy slot is reused after)
@@ -316,6 +326,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tmem_ld32(t_dp + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32 * c]));
         }
         tmem_wait_ld();
+        tr(3);
         const int kbase = j * kTileRows + C::kKC * g;  // first key of this warpgroup's columns
         const bool edge = (CAUSAL && j == i) || (kbase + C::kKC > N);
         const uint64_t nl2x2 = f2_pack(nl2, nl2);
@@ -344,6 +355,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ds_full[g]);
+        tr(5);
       }
       if (!ok) break;
       // ---- epilogue: this warpgroup's half of the dQ columns -> scale * dQ, bf16 ----
@@ -408,3 +420,8 @@ cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t stream) {
 int bwd_dq_units(int BH, int N) { return BH * ((N + kTileRows - 1) / kTileRows); }
 
 }  // namespace fa
+
+#ifdef FA_TRACE
+// Trace builds only: phase records of this file's kernel.
+extern "C" int fa_trace_dump_dq(void* host, size_t bytes) { return fa::trace_dump(host, bytes); }
+#endif
