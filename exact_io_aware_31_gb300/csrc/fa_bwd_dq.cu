@@ -13,16 +13,17 @@
 // and at the end of the unit dQ = scale * dQ -> bf16.
 //
 // Roles (10 warps): two compute warpgroups (thread = query row, warpgroup g
-// owning keys [64 g, 64 g + 64) of every key tile: its S and dP columns, and
-// its dS packed as bf16 pairs over the first half of its own S columns), one
-// TMA producer warp (Q, dO and their lse2 / D rows per unit; K, V per key
-// tile through a ring), one MMA warp that owns the TMEM (S [0,128),
-// dP [128,256), dQ [256, 256 + d)).
-// The two key halves of a tile are separate MMAs with their own barriers, so
-// one warpgroup's dS overlaps the other half's MMAs.  Issue order:
-//     S_0 dP_0 | S_1 dP_1 | dQ += dS_0 K_0 | S_0 dP_0 (next tile) | dQ += dS_1 K_1 | S_1 dP_1 (next) ...
-// (each S_g of the next tile follows the dQ MMA that read dS_g from its
-// columns; the tensor pipe runs them in issue order).
+// owning key columns [64 g, 64 g + 64) of S and dP; its dS goes, packed as
+// bf16 pairs, over the first half of its own S columns), one TMA producer
+// warp (Q, dO and their lse2 / D rows per unit; K, V per key tile through a
+// ring), one MMA warp that owns the TMEM: two S banks (key tile j in bank
+// j % 2, at columns 0 and 384 at d = 128), dP [128, 256), dQ [256, 256 + d).
+// The compute warps release dP as soon as S and dP are in their registers,
+// so S and dP of tile j + 1 run on the tensor pipe while dS of tile j is
+// computed; dQ += dS_j K_j follows, then S of tile j + 2 over bank j % 2.
+// Every MMA here reads one operand from shared memory at up to 128 bytes a
+// clock (S and dP both), so keeping the pipe fed, not splitting the MMAs
+// (which re-reads Q per part), is what shortens a tile.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -47,9 +48,11 @@ struct DqCfg {
   static constexpr int kQStages = (D == 64) ? 2 : 1;      // Q / dO / rows of a unit
   static constexpr int kKvStages = (D == 64) ? 3 : 2;     // K / V ring
   static constexpr int kTmemCols = 512;
-  static constexpr int kColS = 0;
+  static constexpr int kColS = 0;                     // S bank 0
   static constexpr int kColDP = 128;
   static constexpr int kColDQ = 256;
+  static constexpr int kColS1 = 256 + D;              // S bank 1 (d = 64 leaves 192 columns)
+  static constexpr int col_s(int bank) { return bank ? kColS1 : kColS; }
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
   static constexpr int kOffK = kOffDO + kQStages * kTileBytes;
@@ -57,12 +60,12 @@ struct DqCfg {
   static constexpr int kOffRow = kOffV + kKvStages * kTileBytes;  // [q stages][-lse2 128 | -D 128] fp32
   static constexpr int kRowBytes = 2 * kTileRows * 4;
   static constexpr int kOffBar = kOffRow + kQStages * kRowBytes;
-  static constexpr int kNumBars = 2 * kQStages + 2 * kKvStages + 7;
+  static constexpr int kNumBars = 2 * kQStages + 2 * kKvStages + 6;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kColDQ + D <= kTmemCols, "tensor memory budget");
+  static_assert(kColS1 + 128 <= kTmemCols, "tensor memory budget");
 };
 
 // Unit `pos`: (b, h) slice and query tile; under the causal mask the tiles
@@ -98,11 +101,12 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   uint64_t* q_empty = q_full + C::kQStages;        // [q stages]
   uint64_t* kv_full = q_empty + C::kQStages;       // [kv stages]
   uint64_t* kv_empty = kv_full + C::kKvStages;     // [kv stages]
-  uint64_t* s_full = kv_empty + C::kKvStages;      // [2] S and dP of key half g in TMEM
-  uint64_t* ds_full = s_full + 2;                  // [2] dS of key half g in TMEM (warpgroup g)
-  uint64_t* dq_full = s_full + 4;                  // the unit's dQ complete
-  uint64_t* dq_empty = s_full + 5;                 // dQ read out (compute threads)
-  uint64_t* mma_done = s_full + 6;
+  uint64_t* s_full = kv_empty + C::kKvStages;      // S and dP of a key tile in TMEM
+  uint64_t* ds_full = s_full + 1;                  // dS of the tile in TMEM (compute threads)
+  uint64_t* dq_full = s_full + 2;                  // the unit's dQ complete
+  uint64_t* dq_empty = s_full + 3;                 // dQ read out (compute threads)
+  uint64_t* mma_done = s_full + 4;
+  uint64_t* dp_free = s_full + 5;                  // S and dP of the tile are in registers (compute threads)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
 
@@ -123,10 +127,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int g = 0; g < C::kWG; ++g) {
-      mbar_init(&s_full[g], 1);
-      mbar_init(&ds_full[g], 128);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(ds_full, C::kComputeThreads);
+    mbar_init(dp_free, C::kComputeThreads);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, C::kComputeThreads);
     mbar_init(mma_done, 1);
@@ -194,12 +197,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer --
     {  // whole warp, converged: waits are warp-wide, one elected lane issues
-      // S_g, dP_g: M = 128 queries, N = 64 keys of half g, A and B K-major over d
-      constexpr uint32_t kIdH = idesc_bf16(128, 64, 0, 0);
-      const uint32_t idS = kIdH | s_negate;                   // S_g = (+/-) Q K_g^T
-      constexpr uint32_t kIdQ = idesc_bf16(128, D, 0, 1);    // dQ += dS_g K_g: A from TMEM, B (K) MN-major
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // S, dP: A and B K-major over d
+      const uint32_t idS = kIdS | s_negate;                   // S = (+/-) Q K^T
+      constexpr uint32_t kIdQ = idesc_bf16(128, D, 0, 1);    // dQ += dS K: A from TMEM, B (K) MN-major
       auto kmajor = [](uint32_t base, int k) { return base + (k / 4) * kSwzBlockBytes + (k % 4) * 32; };
-      uint32_t ucnt = 0, kvit = 0, dscnt = 0, dqcnt = 0;
+      uint32_t ucnt = 0, kvit = 0, dscnt = 0, dqcnt = 0, dpcnt = 0;
       bool ok = true;
       Tracer tr(2);
       for (int round = 0; ok; ++round) {
@@ -213,68 +215,54 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         const uint32_t q_s = smem_addr(sm + C::kOffQ + qs * C::kTileBytes);
         const uint32_t do_s = smem_addr(sm + C::kOffDO + qs * C::kTileBytes);
         if (!(ok = mbar_wait_warp(&q_full[qs], (ucnt / C::kQStages) & 1, status))) break;
-        // S_g and dP_g of key tile `it` (ring slot), keys [64 g, 64 g + 64): the
-        // B operand starts 64 rows (8 swizzle atoms, 8 KiB) into each block.
-        auto issue_half = [&](uint32_t it, int g) {
+        // S = Q K^T into S bank it % 2 and dP = dO V^T of key tile `it` (ring
+        // slot it % stages).  The bank was last read by dQ of tile it - 2,
+        // issued before; dP's columns are rewritten once the compute warps
+        // hold the previous tile's dP in registers.
+        auto issue_sdp = [&](uint32_t it) -> bool {
           const int ks = it % C::kKvStages;
-          const uint32_t k_s = smem_addr(sm + C::kOffK + ks * C::kTileBytes) + 8192u * g;
-          const uint32_t v_s = smem_addr(sm + C::kOffV + ks * C::kTileBytes) + 8192u * g;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(tbase + C::kColS + C::kKC * g, sdesc(kmajor(q_s, k), 16, 1024), sdesc(kmajor(k_s, k), 16, 1024),
-                     idS, k > 0);
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(tbase + C::kColDP + C::kKC * g, sdesc(kmajor(do_s, k), 16, 1024),
-                     sdesc(kmajor(v_s, k), 16, 1024), kIdH, k > 0);
-          mma_commit_w(&s_full[g]);
-        };
-        // dQ += dS_g K_g: A = dS_g (TMEM, over S_g), B = K rows [64 g, 64 g + 64)
-        auto issue_dq = [&](uint32_t it, int g, int j) {
-          const uint32_t k_s = smem_addr(sm + C::kOffK + (it % C::kKvStages) * C::kTileBytes);
-#pragma unroll
-          for (int k = 4 * g; k < 4 * g + 4; ++k)
-            mma_ts_w(tbase + C::kColDQ, tbase + C::kColS + dq_ds_col(k), sdesc(k_s + k * 2048, kSwzBlockBytes, 1024),
-                     kIdQ, (j > 0 || k > 0));
-        };
-        // prologue: both halves of the unit's first key tile
-        if (!(ok = mbar_wait_warp(&kv_full[kvit % C::kKvStages], (kvit / C::kKvStages) & 1, status))) break;
-        tc_fence_after();
-        issue_half(kvit, 0);
-        issue_half(kvit, 1);
-        for (int j = 0; j < nkv && ok; ++j, ++kvit) {
-          const bool more = j + 1 < nkv;
-          // half 0: its dS, then the next tile's S_0, dP_0 (over the dS just read)
+          const uint32_t k_s = smem_addr(sm + C::kOffK + ks * C::kTileBytes);
+          const uint32_t v_s = smem_addr(sm + C::kOffV + ks * C::kTileBytes);
           tr(20);
-          if (!(ok = mbar_wait_warp(&ds_full[0], dscnt & 1, status))) break;
+          if (!mbar_wait_warp(&kv_full[ks], (it / C::kKvStages) & 1, status)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss_w(tbase + C::col_s(it & 1), sdesc(kmajor(q_s, k), 16, 1024), sdesc(kmajor(k_s, k), 16, 1024), idS,
+                     k > 0);
           tr(21);
+          if (dpcnt > 0 && !mbar_wait_warp(dp_free, (dpcnt - 1) & 1, status)) return false;
+          tc_fence_after();
+          tr(22);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss_w(tbase + C::kColDP, sdesc(kmajor(do_s, k), 16, 1024), sdesc(kmajor(v_s, k), 16, 1024), kIdS,
+                     k > 0);
+          ++dpcnt;
+          mma_commit_w(s_full);
+          return true;
+        };
+        if (!(ok = issue_sdp(kvit))) break;  // the unit's first key tile
+        for (int j = 0; j < nkv && ok; ++j, ++kvit) {
+          if (j + 1 < nkv && !(ok = issue_sdp(kvit + 1))) break;
+          // dQ += dS_j K_j, dS_j packed in TMEM over S bank kvit % 2
+          tr(23);
+          if (!(ok = mbar_wait_warp(ds_full, dscnt & 1, status))) break;
+          tr(24);
+          ++dscnt;
           // the first dQ MMA of a unit overwrites the columns: the previous
           // unit's dQ must have been read out
           if (j == 0 && !(ok = mbar_wait_warp(dq_empty, (dqcnt & 1) ^ 1, status))) break;
           tc_fence_after();
-          issue_dq(kvit, 0, j);
-          if (more) {
-            if (!(ok = mbar_wait_warp(&kv_full[(kvit + 1) % C::kKvStages], ((kvit + 1) / C::kKvStages) & 1, status)))
-              break;
-            tc_fence_after();
-            issue_half(kvit + 1, 0);
-          }
-          // half 1
-          tr(22);
-          if (!(ok = mbar_wait_warp(&ds_full[1], dscnt & 1, status))) break;
-          tr(23);
-          ++dscnt;
-          tc_fence_after();
-          issue_dq(kvit, 1, j);
-          mma_commit_w(&kv_empty[kvit % C::kKvStages]);  // K_j, V_j have no later reader
-          if (more) issue_half(kvit + 1, 1);
-          tr(24);
-          // Q and dO have no later reader once the unit's last S_1, dP_1 are
-          // issued, and both warpgroups have read the unit's -lse2 / -D rows
-          // (before their first dS, waited for above): the slot may be reused.
-          if (j + 2 == nkv || nkv == 1) mma_commit_w(&q_empty[qs]);
+          const uint32_t k_s = smem_addr(sm + C::kOffK + (kvit % C::kKvStages) * C::kTileBytes);
+#pragma unroll
+          for (int k = 0; k < kTileRows / 16; ++k)
+            mma_ts_w(tbase + C::kColDQ, tbase + C::col_s(kvit & 1) + dq_ds_col(k),
+                     sdesc(k_s + k * 2048, kSwzBlockBytes, 1024), kIdQ, (j > 0 || k > 0));
+          mma_commit_w(&kv_empty[kvit % C::kKvStages]);
         }
         if (!ok) break;
+        mma_commit_w(&q_empty[qs]);
         mma_commit_w(dq_full);
         ++dqcnt;
         ++ucnt;
@@ -290,7 +278,6 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;  // query row in the tile
     const uint32_t lanes = (uint32_t)quarter * 32;
-    const uint32_t t_s = tmem_lane_col(tbase, lanes, C::kColS + C::kKC * g);
     const uint32_t t_dp = tmem_lane_col(tbase, lanes, C::kColDP + C::kKC * g);
     const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + (D / 2) * g);
     uint32_t ucnt = 0, scnt = 0, dqcnt = 0;
@@ -311,8 +298,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       if (!(ok = mbar_wait_warp(&q_full[qs], (ucnt / C::kQStages) & 1, status))) break;  // the rows are in
       for (int j = 0; j < nkv; ++j) {
         tr(1);
-        if (!(ok = mbar_wait_warp(&s_full[g], scnt & 1, status))) break;
+        if (!(ok = mbar_wait_warp(s_full, scnt & 1, status))) break;
         tr(2);
+        // this key tile's S bank (tiles alternate between the two)
+        const uint32_t t_s = tmem_lane_col(tbase, lanes, C::col_s(scnt & 1) + C::kKC * g);
         ++scnt;
         tc_fence_after();
         if (j == 0) {  // read before the unit's first dS is published (the copy slot is reused after)
@@ -326,6 +315,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tmem_ld32(t_dp + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32 * c]));
         }
         tmem_wait_ld();
+        // S and dP are in registers: the MMA warp may compute the next dP
+        tc_fence_before();
+        mbar_arrive(dp_free);
         tr(3);
         const int kbase = j * kTileRows + C::kKC * g;  // first key of this warpgroup's columns
         const bool edge = (CAUSAL && j == i) || (kbase + C::kKC > N);
@@ -354,7 +346,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         for (int c = 0; c < C::kKC / 32; ++c) tmem_st16(t_s + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&ds_full[g]);
+        mbar_arrive(ds_full);
         tr(5);
       }
       if (!ok) break;
