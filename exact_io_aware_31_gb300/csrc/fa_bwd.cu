@@ -184,6 +184,15 @@ struct BwdCfg {
   // those two to finish reading dS(i).  At d = 128 the dQ^T partial occupies
   // the dP^T columns, so dP^T(i+1) waits until dQ^T(i) has been drained.
   static constexpr bool kEarlyDp = !kDqAliasesDp;
+  // Without dQ (the dK / dV kernel of the deterministic backward), dS is
+  // packed as bf16 pairs into the first half of each warpgroup's own dP^T
+  // columns (read into registers just before) and dK takes its A operand from
+  // tensor memory: shared memory carries neither the dS stores nor the dK
+  // MMA's A reads, 64 KiB a tile pair at d = 128 of a kernel whose MMAs
+  // otherwise read shared memory at its full rate.  dP^T(i+1) overwrites the
+  // columns after dK(i) in issue order.  (dQ needs dS^T as a B operand, which
+  // only shared memory can hold.)
+  static constexpr bool kDsTmem = !DQ;
   static constexpr int kDsBufs = (kEarlyDp && D == 64) ? 2 : 1;  // no room for a second one at d = 128
   static constexpr int kDsBytes = 2 * kSwzBlockBytes;              // 128 x 128 bf16 dS^T, two swizzle blocks
   static constexpr int kOffDS = kOffDO + kStages * kTileBytes;    // [kDsBufs]
@@ -517,10 +526,17 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t dsb = ds_s + db * C::kDsBytes;
+          if constexpr (C::kDsTmem) {  // dK += dS^T Q, dS^T packed over the dP^T columns
 #pragma unroll
-          for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ss_w(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
-                     sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+            for (int k = 0; k < kTileRows / 16; ++k)
+              mma_ts_w(tbase + C::kColDK, tbase + C::kColDP + pt_col<C::kQCols>(k),
+                       sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+          } else {
+#pragma unroll
+            for (int k = 0; k < kTileRows / 16; ++k)
+              mma_ss_w(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
+                       sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+          }
           mma_commit_w(&qdo_empty[st]);  // Q(i), dO(i) read for the last time: the producer may reload the slot
           if (C::kEarlyDp && x + 1 < u.nq) {
             tr(12);
@@ -813,7 +829,13 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
               f2_unpack(f2_mul(f2_pack(pf.x, pf.y), t), d0, d1);
               dsk[e] = pack_bf16x2(d0, d1);
             }
-            *reinterpret_cast<uint4*>(ds_row + (((cbase + m) ^ swz) * 16)) = make_uint4(dsk[0], dsk[1], dsk[2], dsk[3]);
+            if constexpr (C::kDsTmem) {  // P^T is no longer needed: its registers keep dS^T for tensor memory
+#pragma unroll
+              for (int e = 0; e < 4; ++e) pk[4 * m + e] = dsk[e];
+            } else {
+              *reinterpret_cast<uint4*>(ds_row + (((cbase + m) ^ swz) * 16)) =
+                  make_uint4(dsk[0], dsk[1], dsk[2], dsk[3]);
+            }
             if (kDqInterleave && dq_have) {  // the rest, kDqPerChunk per chunk of eight queries
 #pragma unroll
               for (int e4 = 0; e4 < kDqPerChunk; ++e4) {
@@ -823,7 +845,13 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
             }
           }
         }
-        fence_proxy_async_smem();
+        if constexpr (C::kDsTmem) {
+#pragma unroll
+          for (int c = 0; c < kQC / 32; ++c) tmem_st16(t_dp + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
+          tmem_wait_st();
+        } else {
+          fence_proxy_async_smem();
+        }
         tc_fence_before();
         mbar_arrive(ds_full);
         tr(5);

@@ -46,7 +46,11 @@ struct DqCfg {
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
   static constexpr int kQStages = (D == 64) ? 2 : 1;      // Q / dO / rows of a unit
-  static constexpr int kKvStages = (D == 64) ? 3 : 2;     // K / V ring
+  // K and V in rings of their own: V_j is last read by dP_j, early, while K_j
+  // is read until dQ_j at the end of the tile, and S of tile j + 1 is issued
+  // before dQ_j, so the K ring is one deeper to keep its copy ahead.
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = (D == 64) ? 3 : 2;
   static constexpr int kTmemCols = 512;
   static constexpr int kColS = 0;                     // S bank 0
   static constexpr int kColDP = 128;
@@ -56,11 +60,11 @@ struct DqCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
   static constexpr int kOffK = kOffDO + kQStages * kTileBytes;
-  static constexpr int kOffV = kOffK + kKvStages * kTileBytes;
-  static constexpr int kOffRow = kOffV + kKvStages * kTileBytes;  // [q stages][-lse2 128 | -D 128] fp32
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffRow = kOffV + kVStages * kTileBytes;  // [q stages][-lse2 128 | -D 128] fp32
   static constexpr int kRowBytes = 2 * kTileRows * 4;
   static constexpr int kOffBar = kOffRow + kQStages * kRowBytes;
-  static constexpr int kNumBars = 2 * kQStages + 2 * kKvStages + 6;
+  static constexpr int kNumBars = 2 * kQStages + 2 * kKStages + 2 * kVStages + 6;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;
@@ -99,9 +103,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* q_full = bars;                         // [q stages]
   uint64_t* q_empty = q_full + C::kQStages;        // [q stages]
-  uint64_t* kv_full = q_empty + C::kQStages;       // [kv stages]
-  uint64_t* kv_empty = kv_full + C::kKvStages;     // [kv stages]
-  uint64_t* s_full = kv_empty + C::kKvStages;      // S and dP of a key tile in TMEM
+  uint64_t* k_full = q_empty + C::kQStages;        // [K stages]
+  uint64_t* k_empty = k_full + C::kKStages;        // [K stages]
+  uint64_t* v_full = k_empty + C::kKStages;        // [V stages]
+  uint64_t* v_empty = v_full + C::kVStages;        // [V stages]
+  uint64_t* s_full = v_empty + C::kVStages;        // S and dP of a key tile in TMEM
   uint64_t* ds_full = s_full + 1;                  // dS of the tile in TMEM (compute threads)
   uint64_t* dq_full = s_full + 2;                  // the unit's dQ complete
   uint64_t* dq_empty = s_full + 3;                 // dQ read out (compute threads)
@@ -123,9 +129,13 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    for (int s = 0; s < C::kKvStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(ds_full, C::kComputeThreads);
@@ -175,22 +185,26 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         bulk_load_1d(rows + kTileRows, dsum + roff, kTileRows * 4, &q_full[qs]);
         ++ucnt;
         for (int j = 0; j < nkv && ok; ++j, ++kvit) {
-          const int ks = kvit % C::kKvStages;
-          if (!(ok = mbar_wait(&kv_empty[ks], ((kvit / C::kKvStages) & 1) ^ 1, status))) break;
-          mbar_expect_tx(&kv_full[ks], 2 * C::kTileBytes);
-          for (int b = 0; b < C::kBlocks; ++b) {
-            tma_load_3d(sm + C::kOffK + ks * C::kTileBytes + b * kSwzBlockBytes, &tm_k, &kv_full[ks], 64 * b,
+          const int ks = kvit % C::kKStages, vs = kvit % C::kVStages;
+          if (!(ok = mbar_wait(&k_empty[ks], ((kvit / C::kKStages) & 1) ^ 1, status))) break;
+          mbar_expect_tx(&k_full[ks], C::kTileBytes);
+          for (int b = 0; b < C::kBlocks; ++b)
+            tma_load_3d(sm + C::kOffK + ks * C::kTileBytes + b * kSwzBlockBytes, &tm_k, &k_full[ks], 64 * b,
                         j * kTileRows, bh);
-            tma_load_3d(sm + C::kOffV + ks * C::kTileBytes + b * kSwzBlockBytes, &tm_v, &kv_full[ks], 64 * b,
+          if (!(ok = mbar_wait(&v_empty[vs], ((kvit / C::kVStages) & 1) ^ 1, status))) break;
+          mbar_expect_tx(&v_full[vs], C::kTileBytes);
+          for (int b = 0; b < C::kBlocks; ++b)
+            tma_load_3d(sm + C::kOffV + vs * C::kTileBytes + b * kSwzBlockBytes, &tm_v, &v_full[vs], 64 * b,
                         j * kTileRows, bh);
-          }
         }
         if (aborted(abort_flag)) ok = false;
       }
       if (!ok) *abort_flag = 1;
       // Drain copies in flight (bounded).
-      for (uint32_t x = (kvit > (uint32_t)C::kKvStages ? kvit - C::kKvStages : 0); x < kvit; ++x)
-        mbar_wait(&kv_full[x % C::kKvStages], (x / C::kKvStages) & 1, status);
+      for (uint32_t x = (kvit > (uint32_t)C::kKStages ? kvit - C::kKStages : 0); x < kvit; ++x)
+        mbar_wait(&k_full[x % C::kKStages], (x / C::kKStages) & 1, status);
+      for (uint32_t x = (kvit > (uint32_t)C::kVStages ? kvit - C::kVStages : 0); x < kvit; ++x)
+        mbar_wait(&v_full[x % C::kVStages], (x / C::kVStages) & 1, status);
       for (uint32_t x = (ucnt > (uint32_t)C::kQStages ? ucnt - C::kQStages : 0); x < ucnt; ++x)
         mbar_wait(&q_full[x % C::kQStages], (x / C::kQStages) & 1, status);
     }
@@ -220,11 +234,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         // issued before; dP's columns are rewritten once the compute warps
         // hold the previous tile's dP in registers.
         auto issue_sdp = [&](uint32_t it) -> bool {
-          const int ks = it % C::kKvStages;
+          const int ks = it % C::kKStages, vs = it % C::kVStages;
           const uint32_t k_s = smem_addr(sm + C::kOffK + ks * C::kTileBytes);
-          const uint32_t v_s = smem_addr(sm + C::kOffV + ks * C::kTileBytes);
+          const uint32_t v_s = smem_addr(sm + C::kOffV + vs * C::kTileBytes);
           tr(20);
-          if (!mbar_wait_warp(&kv_full[ks], (it / C::kKvStages) & 1, status)) return false;
+          if (!mbar_wait_warp(&k_full[ks], (it / C::kKStages) & 1, status)) return false;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
@@ -232,6 +246,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
                      k > 0);
           tr(21);
           if (dpcnt > 0 && !mbar_wait_warp(dp_free, (dpcnt - 1) & 1, status)) return false;
+          if (!mbar_wait_warp(&v_full[vs], (it / C::kVStages) & 1, status)) return false;
           tc_fence_after();
           tr(22);
 #pragma unroll
@@ -240,6 +255,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
                      k > 0);
           ++dpcnt;
           mma_commit_w(s_full);
+          mma_commit_w(&v_empty[vs]);  // V of this tile has no later reader
           return true;
         };
         if (!(ok = issue_sdp(kvit))) break;  // the unit's first key tile
@@ -254,12 +270,12 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           // unit's dQ must have been read out
           if (j == 0 && !(ok = mbar_wait_warp(dq_empty, (dqcnt & 1) ^ 1, status))) break;
           tc_fence_after();
-          const uint32_t k_s = smem_addr(sm + C::kOffK + (kvit % C::kKvStages) * C::kTileBytes);
+          const uint32_t k_s = smem_addr(sm + C::kOffK + (kvit % C::kKStages) * C::kTileBytes);
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k)
             mma_ts_w(tbase + C::kColDQ, tbase + C::col_s(kvit & 1) + dq_ds_col(k),
                      sdesc(k_s + k * 2048, kSwzBlockBytes, 1024), kIdQ, (j > 0 || k > 0));
-          mma_commit_w(&kv_empty[kvit % C::kKvStages]);
+          mma_commit_w(&k_empty[kvit % C::kKStages]);  // K of this tile has no later reader
         }
         if (!ok) break;
         mma_commit_w(&q_empty[qs]);
