@@ -281,6 +281,11 @@ int decode_cluster_capacity(int dev, int d, int Nq, int size) {
 int decode_plan(int dev, long long bh, int Nq, int Nk, int d, int num_splits, int sms, bool* cluster) {
   const int tiles = (Nk + 127) / 128;
   *cluster = false;
+  if (Nq >= kDecodeMmaMinNq) {  // the tensor-core kernel: splits merge through the workspace
+    if (num_splits > 0) return num_splits < tiles ? num_splits : tiles;
+    long long s0 = sms / bh > 1 ? sms / bh : 1;
+    return (int)(s0 < tiles ? s0 : tiles);
+  }
   if (num_splits > 0) {
     const int s = num_splits < tiles ? num_splits : tiles;
     *cluster = s >= 2 && decode_cluster_capacity(dev, d, Nq, s) >= bh;
@@ -342,9 +347,10 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   if (need > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                    workspace_bytes < need))
     return FA_ERR_WORKSPACE;
-  CUtensorMap tk, tv;
-  if (make_map(&tk, k, BH, Nk, d) || make_map(&tv, v, BH, Nk, d)) return FA_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (make_map(&tq, q, BH, Nq, d) || make_map(&tk, k, BH, Nk, d) || make_map(&tv, v, BH, Nk, d)) return FA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.tm_q = &tq;
   a.tm_k = &tk;
   a.tm_v = &tv;
   a.q = q;

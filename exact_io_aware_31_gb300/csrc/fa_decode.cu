@@ -350,6 +350,298 @@ __global__ void __launch_bounds__(256, (D == 64 && NQ <= 4) ? 2 : 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// fa_decode_mma: the split kernel with the two contractions on the tensor
+// cores, for 3 to 8 queries.  At eight queries the CUDA-core kernel above is
+// bound by its fp32 FMAs (4 Nq d FLOPs a key), not by the cache read.  Here the
+// queries sit in the first rows of a 128-row tile whose other rows are zero
+// (the copy's out-of-range fill), so S = Q K^T and O += P V are ordinary
+// M = 128 tcgen05 MMAs into tensor memory, exactly as in the forward kernel.
+// Per 128-key tile the MMAs take about 1000 tensor-core cycles and read
+// shared memory about 1200 cycles, below the ~2900 cycles an SM needs to
+// stream the tile's 64 KiB of K and V at its share of HBM bandwidth, so the
+// kernel stays bound by the cache read.  Rows past Nq are padding: their
+// probabilities are written as zero, and rows 32-127, which no warp reads,
+// are never stored.
+// Roles (4 warps): warp 0 softmax (thread = query row), warp 1 TMA producer
+// (the query tile once, then K / V tiles through a ring), warp 2 TMEM owner
+// and MMA issuer, warp 3 idle.  Tensor memory: S [0, 128) with P written
+// back over its first 64 columns as bf16 pairs, O [128, 128 + D).  S of the
+// next tile is issued after P V of this one (P aliases S), so the commit that
+// publishes S also proves the previous P V has finished and the softmax may
+// rescale O in place (lazily, as in the forward).  The partial outputs go to
+// the same places as the CUDA-core kernel's (the merge kernel is shared).
+template <int D>
+struct DecMmaCfg {
+  static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kBlocks = D / 64;
+  static constexpr int kStages = 3;
+  static constexpr int kThreads = 128;
+  static constexpr int kTmemCols = 256;
+  static constexpr int kColS = 0;
+  static constexpr int kColO = 128;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(128, 1)
+    fa_decode_mma(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                  float* __restrict__ part_o, float* __restrict__ part_lse2, int BH, int Nq, int Nk, int splits,
+                  float c2, int* status) {
+  using C = DecMmaCfg<D>;
+  // A negative scale arrives as a negative c2: S is computed negated on the
+  // tensor core and the softmax uses |c2| (its maxima are of the raw scores).
+  const uint32_t s_negate = c2 < 0.f ? kIdescNegateA : 0u;
+  c2 = fabsf(c2);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (!smem_base_ok(smem_raw, status)) return;
+  uint8_t* sm = smem_raw;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;                 // [stages]
+  uint64_t* kv_empty = kv_full + C::kStages;    // [stages]
+  uint64_t* s_full = kv_empty + C::kStages;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* o_full = s_full + 2;
+  uint64_t* mma_done = s_full + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffAbort);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.x / splits;
+  const int split = blockIdx.x - bh * splits;
+  const int tiles = (Nk + kTileRows - 1) / kTileRows;
+  const int t0 = (int)((long long)split * tiles / splits);
+  const int t1 = (int)((long long)(split + 1) * tiles / splits);
+  const int nt = t1 - t0;  // >= 1: splits never exceed the tiles
+  const int kend = min(t1 * kTileRows, Nk);
+  const int shift = Nk - Nq;  // bottom-right causal: key j visible to query n iff j <= n + shift
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int st = 0; st < C::kStages; ++st) {
+      mbar_init(&kv_full[st], 1);
+      mbar_init(&kv_empty[st], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 32);
+    mbar_init(o_full, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 1) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      mbar_expect_tx(q_full, C::kTileBytes);
+      for (int b = 0; b < C::kBlocks; ++b)  // rows past Nq arrive zero-filled
+        tma_load_3d(sm + C::kOffQ + b * kSwzBlockBytes, &tm_q, q_full, 64 * b, 0, bh);
+      bool ok = true;
+      int j = 0;
+      for (; j < nt && ok; ++j) {
+        const int st = j % C::kStages;
+        if (!(ok = mbar_wait(&kv_empty[st], ((j / C::kStages) & 1) ^ 1, status))) break;
+        if (aborted(abort_flag)) break;
+        mbar_expect_tx(&kv_full[st], 2 * C::kTileBytes);
+        for (int b = 0; b < C::kBlocks; ++b) {
+          tma_load_3d(sm + C::kOffK + st * C::kTileBytes + b * kSwzBlockBytes, &tm_k, &kv_full[st], 64 * b,
+                      (t0 + j) * kTileRows, bh);
+          tma_load_3d(sm + C::kOffV + st * C::kTileBytes + b * kSwzBlockBytes, &tm_v, &kv_full[st], 64 * b,
+                      (t0 + j) * kTileRows, bh);
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      // every copy this thread started lands before the CTA exits
+      mbar_wait(q_full, 0, status);
+      for (int x = (j > C::kStages ? j - C::kStages : 0); x < j; ++x)
+        mbar_wait(&kv_full[x % C::kStages], (x / C::kStages) & 1, status);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------- MMA issuer --
+    const uint32_t idS = idesc_bf16(128, 128, 0, 0) | s_negate;  // S = (+/-) Q K^T, both K-major
+    constexpr uint32_t kIdO = idesc_bf16(128, D, 0, 1);            // O += P V, V MN-major
+    const uint32_t q_s = smem_addr(sm + C::kOffQ);
+    bool ok = mbar_wait_warp(q_full, 0, status);
+    for (int j = 0; j < nt && ok; ++j) {
+      const int st = j % C::kStages;
+      const uint32_t k_s = smem_addr(sm + C::kOffK + st * C::kTileBytes);
+      const uint32_t v_s = smem_addr(sm + C::kOffV + st * C::kTileBytes);
+      if (!(ok = mbar_wait_warp(&kv_full[st], (j / C::kStages) & 1, status))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
+        mma_ss_w(tbase + C::kColS, sdesc(q_s + off, 16, 1024), sdesc(k_s + off, 16, 1024), idS, k > 0);
+      }
+      mma_commit_w(s_full);
+      if (!(ok = mbar_wait_warp(p_full, j & 1, status))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kTileRows / 16; ++k)
+        mma_ts_w(tbase + C::kColO, tbase + C::kColS + k * 8, sdesc(v_s + k * 2048, kSwzBlockBytes, 1024), kIdO,
+                 (j > 0 || k > 0));
+      mma_commit_w(&kv_empty[st]);
+      if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
+    }
+    if (!ok) *abort_flag = 1;
+    mma_commit_w(o_full);
+    mma_commit_w(mma_done);
+    mbar_wait_warp(mma_done, 0, status);
+  } else if (warp == 0) {
+    // -------------------------------------------------------------- softmax --
+    const int n = lane;  // query row
+    const uint32_t t_s = tmem_lane_col(tbase, 0, C::kColS);
+    const uint32_t t_o = tmem_lane_col(tbase, 0, C::kColO);
+    float m_run = -INFINITY, l_run = 0.f;  // log2 units
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      if (!(ok = mbar_wait_warp(s_full, j & 1, status))) break;
+      tc_fence_after();
+      uint32_t sv[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(t_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
+      tmem_wait_ld();
+      float* s = reinterpret_cast<float*>(sv);
+      // key kbase + c is visible iff c <= cut (cut < 0: none of the tile)
+      const int kbase = (t0 + j) * kTileRows;
+      const int lim = (n < Nq) ? (CAUSAL ? min(kend - 1, n + shift) : kend - 1) : -1;
+      const int cut = lim - kbase;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = (c > cut) ? -INFINITY : s[c];
+      float pm[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) pm[e] = max3f(s[2 * e], s[2 * e + 1], -INFINITY);
+#pragma unroll
+      for (int c = 16; c < 128; c += 2) pm[(c / 2) & 7] = max3f(pm[(c / 2) & 7], s[c], s[c + 1]);
+      const float mx2 =
+          max3f(max3f(pm[0], pm[1], pm[2]), max3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7])) * c2;  // -inf if none
+      if (j == 0) {
+        m_run = mx2;
+      } else {
+        const bool need = mx2 > m_run + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          // O is quiescent: the S commit above covers the previous P V
+          const float m_new = fmaxf(m_run, mx2);
+          const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t v[16];
+            tmem_ld16(t_o + 16 * c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st16(t_o + 16 * c, v);
+          }
+        }
+      }
+      // P = 2^(s c2 - m) (0 where masked; a row that has seen no key yet has
+      // m = -inf and every entry masked), summed in fp32, stored as bf16 pairs
+      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+      const uint64_t c2x2 = f2_pack(c2, c2), negm = f2_pack(-mref, -mref);
+      uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * h + 2 * i;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), c2x2, negm), x0, x1);
+          const uint64_t p = f2_pack(ex2(x0), ex2(x1));
+          ls[i & 3] = f2_add(ls[i & 3], p);
+          float p0, p1;
+          f2_unpack(p, p0, p1);
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(t_s + 16 * h, pk);
+      }
+      {
+        const uint64_t t01 = f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3]));
+        float a0, a1;
+        f2_unpack(t01, a0, a1);
+        l_run += a0 + a1;
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok) ok = mbar_wait_warp(o_full, 0, status);
+    if (!ok) {
+      *abort_flag = 1;
+    } else {
+      tc_fence_after();
+      // this split's output row: normalised O and the base-2 logsumexp
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      const float lse2 = (l_run > 0.f) ? m_run + __log2f(l_run) : -INFINITY;
+      const size_t row = (size_t)bh * Nq + n;
+      const size_t prow = (size_t)split * BH * Nq + row;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(t_o + 32 * c, v);
+        tmem_wait_ld();
+        if (n < Nq) {
+          if (splits == 1) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+            uint4* dst = reinterpret_cast<uint4*>(o + row * D + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(part_o + prow * D + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
+                                   __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
+          }
+        }
+      }
+      if (n < Nq) {
+        if (splits == 1)
+          lse[row] = lse2 * kLn2;
+        else
+          part_lse2[prow] = lse2;
+      }
+      tc_fence_before();
+    }
+  }
+  // The merge kernel (a programmatic dependent) may start launching; it
+  // waits for this grid's results before reading them.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, C::kTmemCols);
+  }
+}
+
 // One warp per (b, h, query): merge the splits' partial outputs.
 template <int D>
 __global__ void __launch_bounds__(128) fa_decode_combine(const float* __restrict__ part_o,
@@ -471,12 +763,30 @@ static cudaError_t launch_split_nq(const DecLaunch& a, cudaStream_t stream) {
   return launch_split_t<D, 8, CAUSAL>(a, stream);
 }
 
+template <int D, bool CAUSAL>
+static cudaError_t launch_mma_t(const DecLaunch& a, cudaStream_t stream) {
+  using C = DecMmaCfg<D>;
+  auto kern = fa_decode_mma<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<a.BH * a.splits, C::kThreads, C::kSmemBytes, stream>>>(
+      *a.tm_q, *a.tm_k, *a.tm_v, reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, a.part_o, a.part_lse2, a.BH, a.Nq,
+      a.Nk, a.splits, a.c2, a.status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecLaunch& a, cudaStream_t stream) {
   cudaError_t e;
-  if (a.d == 64)
+  if (a.Nq >= kDecodeMmaMinNq) {  // tensor-core contractions (never a cluster)
+    if (a.d == 64)
+      e = a.causal ? launch_mma_t<64, true>(a, stream) : launch_mma_t<64, false>(a, stream);
+    else
+      e = a.causal ? launch_mma_t<128, true>(a, stream) : launch_mma_t<128, false>(a, stream);
+  } else if (a.d == 64) {
     e = a.causal ? launch_split_nq<64, true>(a, stream) : launch_split_nq<64, false>(a, stream);
-  else
+  } else {
     e = a.causal ? launch_split_nq<128, true>(a, stream) : launch_split_nq<128, false>(a, stream);
+  }
   if (e != cudaSuccess || a.splits == 1 || a.cluster) return e;
   const int rows = a.BH * a.Nq;
   cudaLaunchConfig_t cfg = {};

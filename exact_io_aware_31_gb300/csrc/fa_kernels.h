@@ -57,6 +57,7 @@ struct BwdLaunch {
 
 // Split-KV forward (decode): Nq <= 8 queries per head against Nk keys.
 struct DecLaunch {
+  const CUtensorMap* tm_q;  // [BH, Nq, d] bf16, 64-column x 128-row boxes (rows past Nq read as zero)
   const CUtensorMap* tm_k;  // [BH, Nk, d] bf16, 64-column x 128-row boxes
   const CUtensorMap* tm_v;
   const void* q;            // [BH, Nq, d] bf16
@@ -74,6 +75,9 @@ struct DecLaunch {
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecLaunch& a, cudaStream_t stream);
+// Queries from which the split-KV forward runs its contractions on the tensor
+// cores (fewer run on the CUDA cores).
+constexpr int kDecodeMmaMinNq = 3;
 // Clusters of `cluster` decode split CTAs that can be resident at once (0: none).
 int decode_max_clusters(int d, int nq, int causal, int cluster);
 cudaError_t launch_bwd_pre(const BwdLaunch& a, cudaStream_t stream);
