@@ -281,11 +281,6 @@ int decode_cluster_capacity(int dev, int d, int Nq, int size) {
 int decode_plan(int dev, long long bh, int Nq, int Nk, int d, int num_splits, int sms, bool* cluster) {
   const int tiles = (Nk + 127) / 128;
   *cluster = false;
-  if (Nq >= kDecodeMmaMinNq) {  // the tensor-core kernel: splits merge through the workspace
-    if (num_splits > 0) return num_splits < tiles ? num_splits : tiles;
-    long long s0 = sms / bh > 1 ? sms / bh : 1;
-    return (int)(s0 < tiles ? s0 : tiles);
-  }
   if (num_splits > 0) {
     const int s = num_splits < tiles ? num_splits : tiles;
     *cluster = s >= 2 && decode_cluster_capacity(dev, d, Nq, s) >= bh;

@@ -369,8 +369,10 @@ __global__ void __launch_bounds__(256, (D == 64 && NQ <= 4) ? 2 : 1)
 // back over its first 64 columns as bf16 pairs, O [128, 128 + D).  S of the
 // next tile is issued after P V of this one (P aliases S), so the commit that
 // publishes S also proves the previous P V has finished and the softmax may
-// rescale O in place (lazily, as in the forward).  The partial outputs go to
-// the same places as the CUDA-core kernel's (the merge kernel is shared).
+// rescale O in place (lazily, as in the forward).  The splits merge as in the
+// CUDA-core kernel: inside a cluster through distributed shared memory (the
+// query tile's buffer, free once the last MMA is done, holds each split's
+// partial), or through the workspace and the shared merge kernel.
 template <int D>
 struct DecMmaCfg {
   static constexpr int kTileBytes = kTileRows * D * 2;
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(128, 1)
     fa_decode_mma(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                   float* __restrict__ part_o, float* __restrict__ part_lse2, int BH, int Nq, int Nk, int splits,
-                  float c2, int* status) {
+                  int cluster_merge, float c2, int* status) {
   using C = DecMmaCfg<D>;
   // A negative scale arrives as a negative c2: S is computed negated on the
   // tensor core and the softmax uses |c2| (its maxima are of the raw scores).
@@ -598,13 +600,17 @@ __global__ void __launch_bounds__(128, 1)
       const float lse2 = (l_run > 0.f) ? m_run + __log2f(l_run) : -INFINITY;
       const size_t row = (size_t)bh * Nq + n;
       const size_t prow = (size_t)split * BH * Nq + row;
+      float* mrg = reinterpret_cast<float*>(sm + C::kOffQ);  // [8][D] partial rows + [8] lse2 (cluster merge)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(t_o + 32 * c, v);
         tmem_wait_ld();
         if (n < Nq) {
-          if (splits == 1) {
+          if (cluster_merge) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mrg[n * D + 32 * c + i] = __uint_as_float(v[i]) * inv;
+          } else if (splits == 1) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -622,13 +628,57 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
       if (n < Nq) {
-        if (splits == 1)
+        if (cluster_merge)
+          mrg[8 * D + n] = lse2;
+        else if (splits == 1)
           lse[row] = lse2 * kLn2;
         else
           part_lse2[prow] = lse2;
       }
       tc_fence_before();
     }
+  }
+  if (cluster_merge) {
+    // The splits of this head form one cluster (rank = split) and merge their
+    // partials through distributed shared memory with the online-softmax
+    // rescale (weights 2^(lse2_r - max)).  Every rank writes a slice of the
+    // head's output: it first forms the weights of each query from all ranks'
+    // lse2, then sums its elements over the ranks.  Every thread of every CTA
+    // takes both cluster barriers, also after a timeout (the output is then
+    // void and the status word says so).
+    cluster_sync_all();
+    const uint32_t mrg_addr = smem_addr(sm + C::kOffQ);
+    float* wts = reinterpret_cast<float*>(sm + C::kOffK);  // [8][16] weights, [8] 1 / l, [8] m (K ring is free)
+    const int t = threadIdx.x;
+    if (t < Nq) {
+      float m = -INFINITY;
+      for (int r = 0; r < splits; ++r) m = fmaxf(m, ld_cluster_f32(mrg_addr + (8 * D + t) * 4, r));
+      float l = 0.f;
+      for (int r = 0; r < splits; ++r) {
+        const float x = ld_cluster_f32(mrg_addr + (8 * D + t) * 4, r);
+        const float w = (x == -INFINITY) ? 0.f : ex2(x - m);
+        wts[t * 16 + r] = w;
+        l += w;
+      }
+      wts[128 + t] = 1.f / l;
+      wts[136 + t] = m;
+    }
+    __syncthreads();
+    const int rank = (int)cluster_rank();
+    const int total = Nq * D;
+    const int chunk = (total + splits - 1) / splits;
+    const int i1 = min(total, (rank + 1) * chunk);
+    if (!aborted(abort_flag)) {
+      for (int i = rank * chunk + t; i < i1; i += C::kThreads) {
+        const int n = i / D;
+        float v = 0.f;
+        for (int r = 0; r < splits; ++r) v = fmaf(wts[n * 16 + r], ld_cluster_f32(mrg_addr + i * 4, r), v);
+        const size_t row = (size_t)bh * Nq + n;
+        o[row * D + (i - n * D)] = __float2bfloat16_rn(v * wts[128 + n]);
+        if (i - n * D == 0) lse[row] = (wts[136 + n] - __log2f(wts[128 + n])) * kLn2;
+      }
+    }
+    cluster_sync_all();  // keep every CTA's shared memory alive until the others have read it
   }
   // The merge kernel (a programmatic dependent) may start launching; it
   // waits for this grid's results before reading them.
@@ -749,8 +799,15 @@ static int max_clusters_nq(int nq, int cluster) {
   return max_clusters_t<D, 8, CAUSAL>(cluster);
 }
 
+template <int D, bool CAUSAL>
+static int max_clusters_mma_t(int cluster);
+
 int decode_max_clusters(int d, int nq, int causal, int cluster) {
   if (cluster < 2 || cluster > 16) return 0;
+  if (nq >= kDecodeMmaMinNq) {
+    if (d == 64) return causal ? max_clusters_mma_t<64, true>(cluster) : max_clusters_mma_t<64, false>(cluster);
+    return causal ? max_clusters_mma_t<128, true>(cluster) : max_clusters_mma_t<128, false>(cluster);
+  }
   if (d == 64) return causal ? max_clusters_nq<64, true>(nq, cluster) : max_clusters_nq<64, false>(nq, cluster);
   return causal ? max_clusters_nq<128, true>(nq, cluster) : max_clusters_nq<128, false>(nq, cluster);
 }
@@ -764,15 +821,61 @@ static cudaError_t launch_split_nq(const DecLaunch& a, cudaStream_t stream) {
 }
 
 template <int D, bool CAUSAL>
-static cudaError_t launch_mma_t(const DecLaunch& a, cudaStream_t stream) {
+static cudaError_t prepare_mma_t(int cluster) {
   using C = DecMmaCfg<D>;
   auto kern = fa_decode_mma<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e == cudaSuccess && cluster > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_mma_t(const DecLaunch& a, cudaStream_t stream) {
+  using C = DecMmaCfg<D>;
+  cudaError_t e = prepare_mma_t<D, CAUSAL>(a.cluster ? a.splits : 1);
   if (e != cudaSuccess) return e;
-  kern<<<a.BH * a.splits, C::kThreads, C::kSmemBytes, stream>>>(
-      *a.tm_q, *a.tm_k, *a.tm_v, reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, a.part_o, a.part_lse2, a.BH, a.Nq,
-      a.Nk, a.splits, a.c2, a.status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.BH * a.splits);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of one head form a cluster
+  attr[0].val.clusterDim.x = a.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.cluster ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fa_decode_mma<D, CAUSAL>, *a.tm_q, *a.tm_k, *a.tm_v,
+                            reinterpret_cast<__nv_bfloat16*>(a.o), a.lse, a.part_o, a.part_lse2, a.BH, a.Nq, a.Nk,
+                            a.splits, a.cluster, a.c2, a.status);
+}
+
+// Clusters of `cluster` tensor-core decode CTAs resident at once (0: none).
+template <int D, bool CAUSAL>
+static int max_clusters_mma_t(int cluster) {
+  using C = DecMmaCfg<D>;
+  if (prepare_mma_t<D, CAUSAL>(cluster) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fa_decode_mma<D, CAUSAL>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 cudaError_t launch_decode(const DecLaunch& a, cudaStream_t stream) {
