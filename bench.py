@@ -57,7 +57,7 @@ class L2Flush:
 
     def __call__(self):
         self.w.zero_()
-        torch.sum(self.r, out=self.sink)
+        torch.sum(self.r, dim=0, out=self.sink)
 
 
 def flops_per_step(w):
