@@ -168,7 +168,20 @@ struct BwdCfg {
   static constexpr int kProducerWarp = kComputeWarps;
   static constexpr int kMmaWarp = kComputeWarps + 1;
   static constexpr int kDqWarp0 = kComputeWarps + 2;  // first warp of the dQ warpgroup
-  static constexpr int kThreads = 32 * (kComputeWarps + 2 + (kDqWarpgroup ? 4 : 0));
+  // d = 128 with dQ: 20 warps (four compute warpgroups and one of producer,
+  // MMA issuer and two idle warps), launched at 96 registers a thread (five
+  // warps on each SM sub-partition, one of each warpgroup); the last
+  // warpgroup gives registers back (64) and the compute warps take them
+  // (104): their held dQ values and dS loop otherwise spill into local
+  // memory, through the same LSU path the dQ reductions take.
+  // 4 x 128 x 104 + 128 x 64 = 640 x 96, on the block and on every
+  // sub-partition.  (Without dQ the 96 registers suffice.)
+  static constexpr bool kRegSplit = (D == 128) && DQ;
+  static constexpr int kThreads = kRegSplit ? 640 : 32 * (kComputeWarps + 2 + (kDqWarpgroup ? 4 : 0));
+  static constexpr int kLaunchRegs = 96;
+  static constexpr int kAuxRegs = 64;
+  static constexpr int kComputeRegs = 104;
+  static_assert(!kRegSplit || 4 * 128 * kComputeRegs + 128 * kAuxRegs <= kThreads * kLaunchRegs, "register split");
   static constexpr int kTmemCols = 512;
   static constexpr int kColS = 0;     // S^T; P^T of warpgroup g over columns [kQCols g, kQCols g + kQCols / 2)
   static constexpr int kColDP = 128;  // dP^T
@@ -332,6 +345,11 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  // Each role's code starts with its warpgroup's register budget (d = 128):
+  // the warps from the producer on (producer, MMA issuer, idle) give
+  // registers back and the compute warpgroups take them.
+  if (warp >= C::kComputeWarps) {
+    if constexpr (C::kRegSplit) regs_dec<C::kAuxRegs>();
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
@@ -577,7 +595,81 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
       mma_commit_w(mma_done);
       mbar_wait_warp(mma_done, 0, status);
     }
-  } else if (warp < C::kComputeWarps) {
+  } else if (C::kDqWarpgroup) {
+    // ----------------------------------------------------- dQ warpgroup --
+    // d = 64 only: thread = query row r; it reads its 64-column dQ row, releases
+    // the columns, writes the row into a pair of 128-byte-swizzled 32-column
+    // boxes, and one thread issues the tensor reduce-adds.
+    const int quarter = warp % 4;
+    const int r = quarter * 32 + lane;
+    const uint32_t t_dq = tmem_lane_col(tbase, quarter * 32, C::kColDQ);
+    const bool elected = (warp == C::kDqWarp0) && (lane == 0);
+    uint32_t qcnt = 0;
+    bool ok = true;
+    Tracer tr(warp == C::kDqWarp0 + 2 ? 1 : -1);
+    for (int round = 0; ok; ++round) {
+      if (round * grid >= total_units) break;
+      const int pos = snake_unit(round, blockIdx.x, grid);
+      if (pos >= total_units) continue;
+      const BwdUnit u = bwd_decode(pos, BH, nkt, CAUSAL, block_major);
+      for (int x = 0; x < u.nq && ok; ++x) {
+        tr(40);
+        ok = mbar_wait_warp(dq_full, qcnt & 1, status);
+        ++qcnt;
+        if (!ok) break;
+        tc_fence_after();
+        {
+          uint8_t* stage = sm + C::kOffDQS;
+          if (elected) {
+            tma_store_wait_read0();  // the previous reduce-adds have read the buffer
+            mbar_arrive(dqs_free);
+          }
+          if (!(ok = mbar_wait_warp(dqs_free, (qcnt - 1) & 1, status))) break;
+          // Both 32-column halves at once; with 4 compute warpgroups (fewer
+          // registers per thread) one half at a time.
+          constexpr int kHalvesAtOnce = (C::kWG == 4) ? 1 : 2;
+          const int swz = r & 7;
+#pragma unroll
+          for (int b0 = 0; b0 < 2; b0 += kHalvesAtOnce) {
+            uint32_t v[32 * kHalvesAtOnce];
+#pragma unroll
+            for (int h = 0; h < kHalvesAtOnce; ++h)
+              tmem_ld32(t_dq + 32 * (b0 + h), *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+            tmem_wait_ld();
+            if (b0 + kHalvesAtOnce == 2) {  // the whole row is read: release the columns
+              tc_fence_before();
+              mbar_arrive(dq_empty);
+              tr(41);
+            }
+#pragma unroll
+            for (int h = 0; h < kHalvesAtOnce; ++h)
+#pragma unroll
+              for (int m = 0; m < 8; ++m)
+                *reinterpret_cast<uint4*>(stage + (b0 + h) * (C::kDqStageBytes / 2) + r * 128 + ((m ^ swz) * 16)) =
+                    make_uint4(v[32 * h + 4 * m], v[32 * h + 4 * m + 1], v[32 * h + 4 * m + 2],
+                               v[32 * h + 4 * m + 3]);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(dqs_full);
+          if (warp == C::kDqWarp0) {
+            if (!(ok = mbar_wait_warp(dqs_full, (qcnt - 1) & 1, status))) break;
+            if (lane == 0) {
+              for (int b = 0; b < 2; ++b)
+                tma_reduce_add_3d(&tm_dqacc, stage + b * (C::kDqStageBytes / 2), 32 * b, u.qtile(x) * kTileRows,
+                                  u.bh);
+              tma_store_commit();
+            }
+          }
+        }
+        tr(42);
+      }
+      if (aborted(abort_flag)) ok = false;
+    }
+    if (!ok) *abort_flag = 1;
+    if (elected) tma_store_wait_all0();  // reductions in flight land before the CTA exits
+    }
+  } else {
+    if constexpr (C::kRegSplit) regs_inc<C::kComputeRegs>();
     // ------------------------------------------------ compute warpgroups --
     // Warpgroup g owns query columns [kQCols g, kQCols (g+1)) of P^T / dS^T
     // (and of the dQ^T partial at d = 128), and columns [kDCols g,
@@ -949,80 +1041,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     if (!ok) *abort_flag = 1;
     // dK / dV stores still in flight must finish before the CTA exits.
     if (C::kEpiTma && warp == 0 && lane == 0) tma_store_wait_all0();
-  } else if (C::kDqWarpgroup) {
-    // ----------------------------------------------------- dQ warpgroup --
-    // d = 64 only: thread = query row r; it reads its 64-column dQ row, releases
-    // the columns, writes the row into a pair of 128-byte-swizzled 32-column
-    // boxes, and one thread issues the tensor reduce-adds.
-    const int quarter = warp % 4;
-    const int r = quarter * 32 + lane;
-    const uint32_t t_dq = tmem_lane_col(tbase, quarter * 32, C::kColDQ);
-    const bool elected = (warp == C::kDqWarp0) && (lane == 0);
-    uint32_t qcnt = 0;
-    bool ok = true;
-    Tracer tr(warp == C::kDqWarp0 + 2 ? 1 : -1);
-    for (int round = 0; ok; ++round) {
-      if (round * grid >= total_units) break;
-      const int pos = snake_unit(round, blockIdx.x, grid);
-      if (pos >= total_units) continue;
-      const BwdUnit u = bwd_decode(pos, BH, nkt, CAUSAL, block_major);
-      for (int x = 0; x < u.nq && ok; ++x) {
-        tr(40);
-        ok = mbar_wait_warp(dq_full, qcnt & 1, status);
-        ++qcnt;
-        if (!ok) break;
-        tc_fence_after();
-        {
-          uint8_t* stage = sm + C::kOffDQS;
-          if (elected) {
-            tma_store_wait_read0();  // the previous reduce-adds have read the buffer
-            mbar_arrive(dqs_free);
-          }
-          if (!(ok = mbar_wait_warp(dqs_free, (qcnt - 1) & 1, status))) break;
-          // Both 32-column halves at once; with 4 compute warpgroups (fewer
-          // registers per thread) one half at a time.
-          constexpr int kHalvesAtOnce = (C::kWG == 4) ? 1 : 2;
-          const int swz = r & 7;
-#pragma unroll
-          for (int b0 = 0; b0 < 2; b0 += kHalvesAtOnce) {
-            uint32_t v[32 * kHalvesAtOnce];
-#pragma unroll
-            for (int h = 0; h < kHalvesAtOnce; ++h)
-              tmem_ld32(t_dq + 32 * (b0 + h), *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
-            tmem_wait_ld();
-            if (b0 + kHalvesAtOnce == 2) {  // the whole row is read: release the columns
-              tc_fence_before();
-              mbar_arrive(dq_empty);
-              tr(41);
-            }
-#pragma unroll
-            for (int h = 0; h < kHalvesAtOnce; ++h)
-#pragma unroll
-              for (int m = 0; m < 8; ++m)
-                *reinterpret_cast<uint4*>(stage + (b0 + h) * (C::kDqStageBytes / 2) + r * 128 + ((m ^ swz) * 16)) =
-                    make_uint4(v[32 * h + 4 * m], v[32 * h + 4 * m + 1], v[32 * h + 4 * m + 2],
-                               v[32 * h + 4 * m + 3]);
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(dqs_full);
-          if (warp == C::kDqWarp0) {
-            if (!(ok = mbar_wait_warp(dqs_full, (qcnt - 1) & 1, status))) break;
-            if (lane == 0) {
-              for (int b = 0; b < 2; ++b)
-                tma_reduce_add_3d(&tm_dqacc, stage + b * (C::kDqStageBytes / 2), 32 * b, u.qtile(x) * kTileRows,
-                                  u.bh);
-              tma_store_commit();
-            }
-          }
-        }
-        tr(42);
-      }
-      if (aborted(abort_flag)) ok = false;
-    }
-    if (!ok) *abort_flag = 1;
-    if (elected) tma_store_wait_all0();  // reductions in flight land before the CTA exits
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == C::kMmaWarp) {
@@ -1036,6 +1055,15 @@ template <int D, bool CAUSAL, bool DQ, bool DROP = false>
 static cudaError_t launch_main_t(const BwdLaunch& a, cudaStream_t stream) {
   using C = BwdCfg<D, DQ>;
   auto kern = fa_bwd_main<D, CAUSAL, DQ, DROP>;
+  if constexpr (C::kRegSplit) {
+    // The register split assumes a build at exactly kLaunchRegs registers a
+    // thread: with fewer, the compute warpgroups' request could never be met.
+    static const bool regs_ok = [&] {
+      cudaFuncAttributes fa_attr;
+      return cudaFuncGetAttributes(&fa_attr, kern) == cudaSuccess && fa_attr.numRegs == C::kLaunchRegs;
+    }();
+    if (!regs_ok) return cudaErrorInvalidKernelImage;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<a.grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk,
