@@ -12,9 +12,9 @@
 //     dQ += dS K_j                                     (A = dS from TMEM)
 // and at the end of the unit dQ = scale * dQ -> bf16.
 //
-// Roles: compute warpgroups (four at d = 128, two at d = 64; thread = query
-// row, warpgroup g owning key columns [KC g, KC g + KC) of S and dP, its dS
-// packed as bf16 pairs over the first half of its own S columns), one TMA producer
+// Roles (10 warps): two compute warpgroups (thread = query row, warpgroup g
+// owning key columns [64 g, 64 g + 64) of S and dP; its dS goes, packed as
+// bf16 pairs, over the first half of its own S columns), one TMA producer
 // warp (Q, dO and their lse2 / D rows per unit; K, V per key tile through a
 // ring), one MMA warp that owns the TMEM: two S banks (key tile j in bank
 // j % 2, at columns 0 and 384 at d = 128), dP [128, 256), dQ [256, 256 + d).
@@ -36,25 +36,13 @@ namespace fa {
 
 template <int D>
 struct DqCfg {
-  // Compute warpgroups: four at d = 128 (32 keys of each tile a thread, more
-  // warps to hide the TMEM-load and MUFU latency of the dS phase), two at
-  // d = 64 (64 keys a thread).
-  static constexpr int kWG = (D == 128) ? 4 : 2;
+  static constexpr int kWG = 2;
   static constexpr int kKC = kTileRows / kWG;             // key columns per compute warpgroup
   static constexpr int kComputeWarps = 4 * kWG;
   static constexpr int kComputeThreads = 32 * kComputeWarps;
   static constexpr int kProducerWarp = kComputeWarps;
   static constexpr int kMmaWarp = kComputeWarps + 1;
-  // d = 128: 20 warps (the four compute warpgroups and one of producer, MMA
-  // issuer and two idle warps) launched at 96 registers a thread; the last
-  // warpgroup gives registers back to the compute warps:
-  // 4 x 128 x kComputeRegs + 128 x kAuxRegs = 640 x 96.
-  static constexpr bool kRegSplit = (D == 128);
-  static constexpr int kThreads = kRegSplit ? 640 : 32 * (kComputeWarps + 2);
-  static constexpr int kLaunchRegs = 96;
-  static constexpr int kAuxRegs = 64;
-  static constexpr int kComputeRegs = 104;
-  static_assert(!kRegSplit || 4 * 128 * kComputeRegs + 128 * kAuxRegs <= kThreads * kLaunchRegs, "register split");
+  static constexpr int kThreads = 32 * (kComputeWarps + 2);
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kBlocks = D / 64;
   static constexpr int kQStages = (D == 64) ? 2 : 1;      // Q / dO / rows of a unit
@@ -96,12 +84,7 @@ __device__ __forceinline__ void dq_decode(int pos, int BH, int nqt, bool causal,
 
 // P^T column (bf16 pairs) holding keys 16 k .. 16 k + 15 (each warpgroup
 // packs its 64 keys into the first 32 of its own 64 S columns).
-// dS column (bf16 pairs) holding keys 16 k .. 16 k + 15: each warpgroup packs
-// its KC keys into the first KC / 2 of its own KC S columns.
-template <int KC>
-__device__ __forceinline__ uint32_t dq_ds_col(int k) {
-  return KC * (k / (KC / 16)) + 8 * (k % (KC / 16));
-}
+__device__ __forceinline__ uint32_t dq_ds_col(int k) { return 64 * (k / 4) + 8 * (k % 4); }
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
@@ -172,9 +155,6 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  // Each role's code starts with its warpgroup's register budget (d = 128).
-  if (warp >= C::kComputeWarps) {
-    if constexpr (C::kRegSplit) regs_dec<C::kAuxRegs>();
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
@@ -293,7 +273,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           const uint32_t k_s = smem_addr(sm + C::kOffK + (kvit % C::kKStages) * C::kTileBytes);
 #pragma unroll
           for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ts_w(tbase + C::kColDQ, tbase + C::col_s(kvit & 1) + dq_ds_col<C::kKC>(k),
+            mma_ts_w(tbase + C::kColDQ, tbase + C::col_s(kvit & 1) + dq_ds_col(k),
                      sdesc(k_s + k * 2048, kSwzBlockBytes, 1024), kIdQ, (j > 0 || k > 0));
           mma_commit_w(&k_empty[kvit % C::kKStages]);  // K of this tile has no later reader
         }
@@ -308,16 +288,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mma_commit_w(mma_done);
       mbar_wait_warp(mma_done, 0, status);
     }
-  }
   } else {
-    if constexpr (C::kRegSplit) regs_inc<C::kComputeRegs>();
     // ------------------------------------------------ compute warpgroups --
     const int g = warp / 4;
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;  // query row in the tile
     const uint32_t lanes = (uint32_t)quarter * 32;
     const uint32_t t_dp = tmem_lane_col(tbase, lanes, C::kColDP + C::kKC * g);
-    const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + (D / C::kWG) * g);
+    const uint32_t t_dq = tmem_lane_col(tbase, lanes, C::kColDQ + (D / 2) * g);
     uint32_t ucnt = 0, scnt = 0, dqcnt = 0;
     bool ok = true;
     Tracer tr((warp % 4) == 0 ? g : -1);
@@ -388,22 +366,22 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         tr(5);
       }
       if (!ok) break;
-      // ---- epilogue: this warpgroup's share of the dQ columns -> scale * dQ, bf16 ----
+      // ---- epilogue: this warpgroup's half of the dQ columns -> scale * dQ, bf16 ----
       if (!(ok = mbar_wait_warp(dq_full, dqcnt & 1, status))) break;
       ++dqcnt;
       tc_fence_after();
       const bool q_ok = q < N;
 #pragma unroll
-      for (int c = 0; c < D / C::kWG / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t v[32];
         tmem_ld32(t_dq + 32 * c, v);
         tmem_wait_ld();
-        if (c == D / C::kWG / 32 - 1) {
+        if (c == D / 64 - 1) {
           tc_fence_before();
           mbar_arrive(dq_empty);
         }
         if (q_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)bh * N + q) * D + (D / C::kWG) * g + 32 * c);
+          uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)bh * N + q) * D + (D / 2) * g + 32 * c);
 #pragma unroll
           for (int m = 0; m < 4; ++m)
             dst[m] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * m]) * scale, __uint_as_float(v[8 * m + 1]) * scale),
@@ -419,7 +397,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       if (aborted(abort_flag)) ok = false;
     }
     if (!ok) *abort_flag = 1;
-    }
+  }
 
   tc_fence_before();
   __syncthreads();
@@ -434,15 +412,6 @@ template <int D, bool CAUSAL>
 static cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t stream) {
   using C = DqCfg<D>;
   auto kern = fa_bwd_dq<D, CAUSAL>;
-  if constexpr (C::kRegSplit) {
-    // The register split assumes a build at exactly kLaunchRegs registers a
-    // thread: with fewer, the compute warpgroups' request could never be met.
-    static const bool regs_ok = [&] {
-      cudaFuncAttributes fa_attr;
-      return cudaFuncGetAttributes(&fa_attr, kern) == cudaSuccess && fa_attr.numRegs == C::kLaunchRegs;
-    }();
-    if (!regs_ok) return cudaErrorInvalidKernelImage;
-  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<a.dq_grid, C::kThreads, C::kSmemBytes, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, a.lse2, a.dsum,
