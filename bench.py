@@ -472,7 +472,10 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         return c0.elapsed_time(c1) / n
     copies(True, True, 1)
-    h2d_ms, d2h_ms, both_ms = copies(True, False, e2e_steps), copies(False, True, e2e_steps), copies(True, True, e2e_steps)
+    # best of three rounds: the host side is shared, and a ceiling is the best the copies can do
+    h2d_ms, d2h_ms, both_ms = (min(t) for t in zip(*[
+        (copies(True, False, e2e_steps), copies(False, True, e2e_steps), copies(True, True, e2e_steps))
+        for _ in range(3)]))
     e2e_ceiling = whole_job_tflops(world, fwd_f + bwd_f, max(ms_per_step, both_ms))
 
     if rank != 0:
