@@ -451,13 +451,13 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
       const uint32_t idST = kIdSS | s_negate;                  // S^T = (+/-) K Q^T
       constexpr uint32_t kIdKV = idesc_bf16(128, D, 0, 1);    // dV, dK: B (dO / Q) MN-major
       constexpr uint32_t kIdQ = idesc_bf16(128, C::kDqTransposed ? 128 : D, 1, 1);  // dQ / dQ^T: A, B MN-major
+      constexpr int kPtRun = C::kQCols / 16;  // 16-query steps with consecutive P^T / dS^T columns
       const uint32_t q_s = smem_addr(sm + C::kOffQ);
       const uint32_t do_s = smem_addr(sm + C::kOffDO);
       const uint32_t ds_s = smem_addr(sm + C::kOffDS);
       uint32_t ucnt = 0, it = 0, pcnt = 0, dscnt = 0, dqcnt = 0;
       bool ok = true;
       Tracer tr(2);
-      auto kmajor = [](uint32_t base, int k) { return base + (k / 4) * kSwzBlockBytes + (k % 4) * 32; };
       for (int round = 0; ok; ++round) {
         if (round * grid >= total_units) break;
         const int pos = snake_unit(round, blockIdx.x, grid);
@@ -468,16 +468,16 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         const uint32_t v_s = smem_addr(sm + C::kOffV + kb * C::kTileBytes);
         auto issue_st = [&](int st) {  // S^T = K Q^T
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(tbase + C::kColS, sdesc(kmajor(k_s, k), 16, 1024),
-                   sdesc(kmajor(q_s + st * C::kTileBytes, k), 16, 1024), idST, k > 0);
+          for (int blk = 0; blk < D / 64; ++blk)  // four K = 16 steps of 32 bytes per 64-column block
+            mma_ss_run_w<4, 2, 2>(tbase + C::kColS, sdesc(k_s + blk * kSwzBlockBytes, 16, 1024),
+                                  sdesc(q_s + st * C::kTileBytes + blk * kSwzBlockBytes, 16, 1024), idST, blk > 0);
           mma_commit_w(s_full);
         };
         auto issue_dp = [&](int st) {  // dP^T = V dO^T
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(tbase + C::kColDP, sdesc(kmajor(v_s, k), 16, 1024),
-                   sdesc(kmajor(do_s + st * C::kTileBytes, k), 16, 1024), kIdSS, k > 0);
+          for (int blk = 0; blk < D / 64; ++blk)
+            mma_ss_run_w<4, 2, 2>(tbase + C::kColDP, sdesc(v_s + blk * kSwzBlockBytes, 16, 1024),
+                                  sdesc(do_s + st * C::kTileBytes + blk * kSwzBlockBytes, 16, 1024), kIdSS, blk > 0);
           mma_commit_w(dp_full);
         };
         tr(10);
@@ -523,9 +523,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ts_w(tbase + C::kColDV, tbase + C::kColS + pt_col<C::kQCols>(k),
-                   sdesc(do_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+          for (int r = 0; r < kTileRows / 16 / kPtRun; ++r)  // runs of kPtRun 16-query steps (pt_col)
+            mma_ts_run_w<kPtRun, 8, 128>(tbase + C::kColDV, tbase + C::kColS + pt_col<C::kQCols>(r * kPtRun),
+                                         sdesc(do_s + st * C::kTileBytes + r * kPtRun * 2048, kSwzBlockBytes, 1024),
+                                         kIdKV, (x > 0 || r > 0));
           tr(19);
           // S^T(i+1) as early as possible
           if (x + 1 < u.nq) {
@@ -546,14 +547,16 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           const uint32_t dsb = ds_s + db * C::kDsBytes;
           if constexpr (C::kDsTmem) {  // dK += dS^T Q, dS^T packed over the dP^T columns
 #pragma unroll
-            for (int k = 0; k < kTileRows / 16; ++k)
-              mma_ts_w(tbase + C::kColDK, tbase + C::kColDP + pt_col<C::kQCols>(k),
-                       sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+            for (int r = 0; r < kTileRows / 16 / kPtRun; ++r)
+              mma_ts_run_w<kPtRun, 8, 128>(tbase + C::kColDK, tbase + C::kColDP + pt_col<C::kQCols>(r * kPtRun),
+                                           sdesc(q_s + st * C::kTileBytes + r * kPtRun * 2048, kSwzBlockBytes, 1024),
+                                           kIdKV, (x > 0 || r > 0));
           } else {
 #pragma unroll
-            for (int k = 0; k < kTileRows / 16; ++k)
-              mma_ss_w(tbase + C::kColDK, sdesc(kmajor(dsb, k), 16, 1024),
-                       sdesc(q_s + st * C::kTileBytes + k * 2048, kSwzBlockBytes, 1024), kIdKV, (x > 0 || k > 0));
+            for (int blk = 0; blk < kTileRows / 64; ++blk)  // dS^T K-major: 32-byte steps in a block; Q: 16 rows
+              mma_ss_run_w<4, 2, 128>(tbase + C::kColDK, sdesc(dsb + blk * kSwzBlockBytes, 16, 1024),
+                                      sdesc(q_s + st * C::kTileBytes + blk * 4 * 2048, kSwzBlockBytes, 1024), kIdKV,
+                                      (x > 0 || blk > 0));
           }
           mma_commit_w(&qdo_empty[st]);  // Q(i), dO(i) read for the last time: the producer may reload the slot
           if (C::kEarlyDp && x + 1 < u.nq) {
@@ -570,15 +573,12 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           if (DQ) {
-#pragma unroll
-            for (int k = 0; k < kTileRows / 16; ++k) {
-              const uint64_t dsd = sdesc(dsb + k * 2048, kSwzBlockBytes, 1024);  // dS^T, 16 keys
-              const uint64_t kd = sdesc(k_s + k * 2048, kSwzBlockBytes, 1024);   // K, 16 keys
-              if (C::kDqTransposed)
-                mma_ss_w(tbase + C::kColDQ, kd, dsd, kIdQ, k > 0);  // dQ^T = K^T dS^T
-              else
-                mma_ss_w(tbase + C::kColDQ, dsd, kd, kIdQ, k > 0);  // dQ = dS K
-            }
+            const uint64_t dsd = sdesc(dsb, kSwzBlockBytes, 1024);  // dS^T, 16 keys (2048 bytes) a step
+            const uint64_t kd = sdesc(k_s, kSwzBlockBytes, 1024);   // K, 16 keys a step
+            if (C::kDqTransposed)
+              mma_ss_run_w<8, 128, 128>(tbase + C::kColDQ, kd, dsd, kIdQ, 0);  // dQ^T = K^T dS^T
+            else
+              mma_ss_run_w<8, 128, 128>(tbase + C::kColDQ, dsd, kd, kIdQ, 0);  // dQ = dS K
             mma_commit_w(dq_full);
           }
           mma_commit_w(db ? ds_empty2 : ds_empty);

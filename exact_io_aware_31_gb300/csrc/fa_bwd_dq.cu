@@ -214,7 +214,6 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // S, dP: A and B K-major over d
       const uint32_t idS = kIdS | s_negate;                   // S = (+/-) Q K^T
       constexpr uint32_t kIdQ = idesc_bf16(128, D, 0, 1);    // dQ += dS K: A from TMEM, B (K) MN-major
-      auto kmajor = [](uint32_t base, int k) { return base + (k / 4) * kSwzBlockBytes + (k % 4) * 32; };
       uint32_t ucnt = 0, kvit = 0, dscnt = 0, dqcnt = 0, dpcnt = 0;
       bool ok = true;
       Tracer tr(2);
@@ -241,18 +240,18 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           if (!mbar_wait_warp(&k_full[ks], (it / C::kKStages) & 1, status)) return false;
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(tbase + C::col_s(it & 1), sdesc(kmajor(q_s, k), 16, 1024), sdesc(kmajor(k_s, k), 16, 1024), idS,
-                     k > 0);
+          for (int blk = 0; blk < D / 64; ++blk)  // four K = 16 steps of 32 bytes per 64-column block
+            mma_ss_run_w<4, 2, 2>(tbase + C::col_s(it & 1), sdesc(q_s + blk * kSwzBlockBytes, 16, 1024),
+                                  sdesc(k_s + blk * kSwzBlockBytes, 16, 1024), idS, blk > 0);
           tr(21);
           if (dpcnt > 0 && !mbar_wait_warp(dp_free, (dpcnt - 1) & 1, status)) return false;
           if (!mbar_wait_warp(&v_full[vs], (it / C::kVStages) & 1, status)) return false;
           tc_fence_after();
           tr(22);
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(tbase + C::kColDP, sdesc(kmajor(do_s, k), 16, 1024), sdesc(kmajor(v_s, k), 16, 1024), kIdS,
-                     k > 0);
+          for (int blk = 0; blk < D / 64; ++blk)
+            mma_ss_run_w<4, 2, 2>(tbase + C::kColDP, sdesc(do_s + blk * kSwzBlockBytes, 16, 1024),
+                                  sdesc(v_s + blk * kSwzBlockBytes, 16, 1024), kIdS, blk > 0);
           ++dpcnt;
           mma_commit_w(s_full);
           mma_commit_w(&v_empty[vs]);  // V of this tile has no later reader
@@ -272,9 +271,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tc_fence_after();
           const uint32_t k_s = smem_addr(sm + C::kOffK + (kvit % C::kKStages) * C::kTileBytes);
 #pragma unroll
-          for (int k = 0; k < kTileRows / 16; ++k)
-            mma_ts_w(tbase + C::kColDQ, tbase + C::col_s(kvit & 1) + dq_ds_col(k),
-                     sdesc(k_s + k * 2048, kSwzBlockBytes, 1024), kIdQ, (j > 0 || k > 0));
+          for (int r = 0; r < 2; ++r)  // runs of four 16-key steps with consecutive dS columns (dq_ds_col)
+            mma_ts_run_w<4, 8, 128>(tbase + C::kColDQ, tbase + C::col_s(kvit & 1) + dq_ds_col(4 * r),
+                                    sdesc(k_s + r * 4 * 2048, kSwzBlockBytes, 1024), kIdQ, (j > 0 || r > 0));
           mma_commit_w(&k_empty[kvit % C::kKStages]);  // K of this tile has no later reader
         }
         if (!ok) break;

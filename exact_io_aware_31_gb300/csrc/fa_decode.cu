@@ -492,17 +492,14 @@ __global__ void __launch_bounds__(128, 1)
       if (!(ok = mbar_wait_warp(&kv_full[st], (j / C::kStages) & 1, status))) break;
       tc_fence_after();
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
-        mma_ss_w(tbase + C::kColS, sdesc(q_s + off, 16, 1024), sdesc(k_s + off, 16, 1024), idS, k > 0);
-      }
+      for (int blk = 0; blk < D / 64; ++blk)  // four K = 16 steps of 32 bytes per 64-column block
+        mma_ss_run_w<4, 2, 2>(tbase + C::kColS, sdesc(q_s + blk * kSwzBlockBytes, 16, 1024),
+                              sdesc(k_s + blk * kSwzBlockBytes, 16, 1024), idS, blk > 0);
       mma_commit_w(s_full);
       if (!(ok = mbar_wait_warp(p_full, j & 1, status))) break;
       tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < kTileRows / 16; ++k)
-        mma_ts_w(tbase + C::kColO, tbase + C::kColS + k * 8, sdesc(v_s + k * 2048, kSwzBlockBytes, 1024), kIdO,
-                 (j > 0 || k > 0));
+      // 16 keys a step: 8 P columns, 16 rows (2048 bytes) of V
+      mma_ts_run_w<8, 8, 128>(tbase + C::kColO, tbase + C::kColS, sdesc(v_s, kSwzBlockBytes, 1024), kIdO, j > 0);
       mma_commit_w(&kv_empty[st]);
       if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
     }

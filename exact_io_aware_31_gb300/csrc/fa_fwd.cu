@@ -334,15 +334,19 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
             ++sis[t];
             const uint32_t qa = q_s + qbuf[t] * C::kQKBytes, ka = k_s + st * C::kQKBytes;
             // 32 bytes of the 128-byte swizzled rows a step: 16 bf16 or 32 E4M3 elements
+            if constexpr (F8) {
   #pragma unroll
-            for (int k = 0; k < D / (F8 ? 32 : 16); ++k) {
-              const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
-              if constexpr (F8)
+              for (int k = 0; k < D / 32; ++k) {
+                const uint32_t off = (k / 4) * kSwzBlockBytes + (k % 4) * 32;
                 mma_ss_f8_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024),
                             idesc_e4m3(128, 128), k > 0);
-              else
-                mma_ss_w(tbase + C::kColS + 128 * t, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), idS,
-                         k > 0);
+              }
+            } else {
+              // each 64-column block: four K = 16 steps of 32 bytes inside the swizzle atom
+  #pragma unroll
+              for (int kb = 0; kb < D / 64; ++kb)
+                mma_ss_run_w<4, 2, 2>(tbase + C::kColS + 128 * t, sdesc(qa + kb * kSwzBlockBytes, 16, 1024),
+                                    sdesc(ka + kb * kSwzBlockBytes, 16, 1024), idS, kb > 0);
             }
             mma_commit_w(&B.s_full[t]);
             return true;
@@ -426,10 +430,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
                 tr(26 + t);
                 tc_fence_after();
                 const uint32_t va = v_s + st * C::kTileBytes;
-  #pragma unroll
-                for (int k = 0; k < kTileRows / 16; ++k)
-                  mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t + k * 8,
-                           sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
+                // 16 keys a step: 8 P columns, 16 rows (2048 bytes) of V
+                mma_ts_run_w<8, 8, 128>(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t,
+                                      sdesc(va, kSwzBlockBytes, 1024), kIdescO, j > 0);
                 mma_commit_w(&B.pv_done[t]);
                 tr(28 + t);
               }
@@ -459,10 +462,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
               tc_fence_after();
               // O_t (+)= P_t V_j : A = P_t from TMEM (8 columns per 16 keys), B = V_j MN-major
               const uint32_t va = v_s + st * C::kTileBytes;
-  #pragma unroll
-              for (int k = 0; k < kTileRows / 16; ++k)
-                mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColS + 128 * t + k * 8,
-                       sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
+              mma_ts_run_w<8, 8, 128>(tbase + C::kColO + D * t, tbase + C::kColS + 128 * t,
+                                    sdesc(va, kSwzBlockBytes, 1024), kIdescO, j > 0);
               tr(28 + t);
               if (j + 1 < u.nkv(t)) {
                 if (!k_next_ready) {
@@ -520,10 +521,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
               tc_fence_after();
               // O_t (+)= P_t V_j : A = P_t from TMEM (8 columns per 16 keys), B = V_j MN-major
               const uint32_t va = v_s + st * C::kTileBytes;
-  #pragma unroll
-              for (int k = 0; k < kTileRows / 16; ++k)
-                mma_ts_w(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t + k * 8,
-                         sdesc(va + k * 2048, kSwzBlockBytes, 1024), kIdescO, (j > 0 || k > 0));
+              mma_ts_run_w<8, 8, 128>(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t,
+                                    sdesc(va, kSwzBlockBytes, 1024), kIdescO, j > 0);
               mma_commit_w(&B.pv_done[t]);
             }
             if (ok) mma_commit_w(&B.v_empty[st]);
