@@ -155,6 +155,12 @@ struct BwdCfg {
   // never waits on them); d = 128: the compute warpgroups drain it with
   // coalesced reductions (a dedicated warpgroup measured slower there).
   static constexpr bool kDqWarpgroup = DQ && !kDqTransposed;
+  // With the dQ warpgroup, that warpgroup also writes each unit's dK and dV
+  // (through its staging buffer, after the unit's last dQ partial), so the
+  // compute warpgroups go straight on to the next unit: at the unit ends of
+  // the causal GPT-2 shape the compute warps' own epilogue took about a
+  // sixth of their time.
+  static constexpr bool kEpiDqWg = kDqWarpgroup;
   // d = 64: dK / dV leave through the dS buffer (free once the unit's last
   // MMAs are done) as two 64-column boxes with TMA stores; at d = 128 they
   // do not fit there and each thread stores its own row.
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
   uint64_t* mma_done = s_full + 9;
   uint64_t* epi_full = s_full + 10;  // d = 64: dK / dV staged in the dS buffer (all compute threads)
   uint64_t* epi_free = s_full + 11;  // d = 64: their stores have read the dS buffer
-  uint64_t* dqs_full = s_full + 12;  // d = 64: a dQ partial staged (128 arrivals)
+  uint64_t* dqs_full = s_full + 12;  // d = 64: a dQ partial (or dK / dV) staged (128 arrivals)
   uint64_t* dqs_free = s_full + 13;  // d = 64: the staging buffer is free
   uint64_t* ds_empty2 = s_full + 14;  // second dS buffer (d = 64)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmemSlot);
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, C::kDqWarpgroup ? 128 : C::kComputeThreads);
     mbar_init(dkdv_full, 1);
-    mbar_init(dkdv_empty, C::kComputeThreads);
+    mbar_init(dkdv_empty, C::kEpiDqWg ? 128 : C::kComputeThreads);
     mbar_init(mma_done, 1);
     mbar_init(epi_full, C::kComputeThreads);
     mbar_init(epi_free, 1);
@@ -604,7 +610,9 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t t_dq = tmem_lane_col(tbase, quarter * 32, C::kColDQ);
     const bool elected = (warp == C::kDqWarp0) && (lane == 0);
-    uint32_t qcnt = 0;
+    uint32_t qcnt = 0;  // dQ partials drained
+    uint32_t stg = 0;   // uses of the staging buffer (dQ partials and dK / dV)
+    uint32_t ucnt = 0;  // units whose dK / dV this warpgroup wrote
     bool ok = true;
     Tracer tr(warp == C::kDqWarp0 + 2 ? 1 : -1);
     for (int round = 0; ok; ++round) {
@@ -624,7 +632,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
             tma_store_wait_read0();  // the previous reduce-adds have read the buffer
             mbar_arrive(dqs_free);
           }
-          if (!(ok = mbar_wait_warp(dqs_free, (qcnt - 1) & 1, status))) break;
+          if (!(ok = mbar_wait_warp(dqs_free, stg & 1, status))) break;
           // Both 32-column halves at once; with 4 compute warpgroups (fewer
           // registers per thread) one half at a time.
           constexpr int kHalvesAtOnce = (C::kWG == 4) ? 1 : 2;
@@ -652,7 +660,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
           fence_proxy_async_smem();
           mbar_arrive(dqs_full);
           if (warp == C::kDqWarp0) {
-            if (!(ok = mbar_wait_warp(dqs_full, (qcnt - 1) & 1, status))) break;
+            if (!(ok = mbar_wait_warp(dqs_full, stg & 1, status))) break;
             if (lane == 0) {
               for (int b = 0; b < 2; ++b)
                 tma_reduce_add_3d(&tm_dqacc, stage + b * (C::kDqStageBytes / 2), 32 * b, u.qtile(x) * kTileRows,
@@ -660,8 +668,59 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
               tma_store_commit();
             }
           }
+          ++stg;
         }
         tr(42);
+      }
+      if (!ok) break;
+      if constexpr (C::kEpiDqWg) {
+        // ---- the unit's dV and dK (x scale) -> bf16 -> two TMA stores ----
+        // Thread r holds key row r: its 64 dV columns go to box 0 of the
+        // staging buffer, its dK columns to box 1 (128-byte-swizzled 64-column
+        // boxes, chunk m of row r at m ^ (r % 8)).  Rows past N are clipped.
+        ok = mbar_wait_warp(dkdv_full, ucnt & 1, status);
+        ++ucnt;
+        if (!ok) break;
+        tc_fence_after();
+        uint8_t* stage = sm + C::kOffDQS;
+        if (elected) {
+          tma_store_wait_read0();  // the last reduce-adds have read the buffer
+          mbar_arrive(dqs_free);
+        }
+        if (!(ok = mbar_wait_warp(dqs_free, stg & 1, status))) break;
+        const int swz = r & 7;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // 0: dV, 1: dK
+          uint32_t v[64];
+          const uint32_t t_acc = tmem_lane_col(tbase, quarter * 32, h ? C::kColDK : C::kColDV);
+          tmem_ld32(t_acc, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(t_acc + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          if (h == 1) {  // both accumulators read: the next unit may overwrite them
+            tc_fence_before();
+            mbar_arrive(dkdv_empty);
+          }
+          const float sc = h ? scale : 1.f;
+          uint8_t* row = stage + h * (C::kDqStageBytes / 2) + r * 128;
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            *reinterpret_cast<uint4*>(row + ((m ^ swz) * 16)) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[8 * m]) * sc, __uint_as_float(v[8 * m + 1]) * sc),
+                           pack_bf16x2(__uint_as_float(v[8 * m + 2]) * sc, __uint_as_float(v[8 * m + 3]) * sc),
+                           pack_bf16x2(__uint_as_float(v[8 * m + 4]) * sc, __uint_as_float(v[8 * m + 5]) * sc),
+                           pack_bf16x2(__uint_as_float(v[8 * m + 6]) * sc, __uint_as_float(v[8 * m + 7]) * sc));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(dqs_full);
+        if (warp == C::kDqWarp0) {
+          if (!(ok = mbar_wait_warp(dqs_full, stg & 1, status))) break;
+          if (lane == 0) {
+            tma_store_3d(&tm_dv, stage, 0, u.j * kTileRows, u.bh);
+            tma_store_3d(&tm_dk, stage + C::kDqStageBytes / 2, 0, u.j * kTileRows, u.bh);
+            tma_store_commit();
+          }
+        }
+        ++stg;
       }
       if (aborted(abort_flag)) ok = false;
     }
@@ -880,7 +939,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         if (ok) ok = mbar_wait_warp(db ? ds_empty2 : ds_empty, ((dse / C::kDsBufs) & 1) ^ 1, status);
         ++dse;
         uint8_t* ds_row = ds_row0 + db * C::kDsBytes;
-        if (ok && C::kEpiTma && epi_pending) {  // the previous unit's dK / dV stores read the buffer
+        if (ok && C::kEpiTma && !C::kEpiDqWg && epi_pending) {  // the previous unit's dK / dV stores read the buffer
           if (warp == 0 && lane == 0) {
             tma_store_wait_read0();
             mbar_arrive(epi_free);
@@ -955,6 +1014,11 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
         pend_qt = u.qtile(u.nq - 1);
       }
       // ---- epilogue: this warpgroup's half of the dV, dK (x scale) columns -> bf16 ----
+      // (with the dQ warpgroup, that warpgroup writes them)
+      if constexpr (C::kEpiDqWg) {
+        if (aborted(abort_flag)) ok = false;
+        continue;
+      }
       tr(6);
       ok = mbar_wait_warp(dkdv_full, ucnt & 1, status);
       ++ucnt;
@@ -1040,7 +1104,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
     if (DQ && ok && pend_qt >= 0) ok = drain_dq(pend_bh, pend_qt);  // reduced at once: no dS loop follows
     if (!ok) *abort_flag = 1;
     // dK / dV stores still in flight must finish before the CTA exits.
-    if (C::kEpiTma && warp == 0 && lane == 0) tma_store_wait_all0();
+    if (C::kEpiTma && !C::kEpiDqWg && warp == 0 && lane == 0) tma_store_wait_all0();
   }
   tc_fence_before();
   __syncthreads();
