@@ -203,15 +203,18 @@ struct BwdCfg {
   // those two to finish reading dS(i).  At d = 128 the dQ^T partial occupies
   // the dP^T columns, so dP^T(i+1) waits until dQ^T(i) has been drained.
   static constexpr bool kEarlyDp = !kDqAliasesDp;
-  // Without dQ (the dK / dV kernel of the deterministic backward), dS is
-  // packed as bf16 pairs into the first half of each warpgroup's own dP^T
-  // columns (read into registers just before) and dK takes its A operand from
-  // tensor memory: shared memory carries neither the dS stores nor the dK
-  // MMA's A reads, 64 KiB a tile pair at d = 128 of a kernel whose MMAs
-  // otherwise read shared memory at its full rate.  dP^T(i+1) overwrites the
-  // columns after dK(i) in issue order.  (dQ needs dS^T as a B operand, which
-  // only shared memory can hold.)
-  static constexpr bool kDsTmem = !DQ;
+  // dS is packed as bf16 pairs into the first half of each warpgroup's own
+  // dP^T columns (read into registers just before) and dK takes its A operand
+  // from tensor memory, so shared memory does not carry the dK MMA's A reads
+  // (32 KiB a tile pair, in kernels whose MMAs otherwise read shared memory
+  // at its full rate).  dP^T(i+1) overwrites those columns after dK(i) in
+  // issue order.  With dQ, dS also goes to shared memory: dQ needs it as a B
+  // operand, which only shared memory can hold.  (Without dQ, the dK / dV
+  // kernel of the deterministic backward, shared memory carries no dS at
+  // all.)  The fused d = 128 kernel keeps dK's A in shared memory: there the
+  // tensor-memory copy measured no faster.
+  static constexpr bool kDsTmem = !DQ || D == 64;
+  static constexpr bool kDsSmem = DQ;
   static constexpr int kDsBufs = (kEarlyDp && D == 64) ? 2 : 1;  // no room for a second one at d = 128
   static constexpr int kDsBytes = 2 * kSwzBlockBytes;              // 128 x 128 bf16 dS^T, two swizzle blocks
   static constexpr int kOffDS = kOffDO + kStages * kTileBytes;    // [kDsBufs]
@@ -983,10 +986,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
             if constexpr (C::kDsTmem) {  // P^T is no longer needed: its registers keep dS^T for tensor memory
 #pragma unroll
               for (int e = 0; e < 4; ++e) pk[4 * m + e] = dsk[e];
-            } else {
+            }
+            if constexpr (C::kDsSmem)
               *reinterpret_cast<uint4*>(ds_row + (((cbase + m) ^ swz) * 16)) =
                   make_uint4(dsk[0], dsk[1], dsk[2], dsk[3]);
-            }
             if (kDqInterleave && dq_have) {  // the rest, kDqPerChunk per chunk of eight queries
 #pragma unroll
               for (int e4 = 0; e4 < kDqPerChunk; ++e4) {
@@ -1000,9 +1003,8 @@ __global__ void __launch_bounds__(BwdCfg<D, DQ>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kQC / 32; ++c) tmem_st16(t_dp + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
           tmem_wait_st();
-        } else {
-          fence_proxy_async_smem();
         }
+        if constexpr (C::kDsSmem) fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(ds_full);
         tr(5);
