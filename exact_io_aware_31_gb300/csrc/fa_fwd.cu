@@ -8,13 +8,13 @@
 // streams K/V tiles past them, writing O once).
 //
 // Work unit: 256 query rows (two 128-row Q tiles, t = 0, 1) of one (b, h).
-// CTA roles (12 warps; warps 10-11 idle without PVW, warp 11 idle with it):
+// CTA roles (12 warps; warp 11 idle, and warp 10 too at d = 128):
 //   warps 0-3  softmax warpgroup for Q tile 0   (thread = one query row)
 //   warps 4-7  softmax warpgroup for Q tile 1
 //   warp  8    TMA producer: Q tiles, then K_j / V_j into a STAGES-deep ring
-//   warp  9    TMEM owner and MMA issuer (one elected lane); with PVW it
-//              issues the S MMAs only
-//   warp 10    (PVW, d = 64) issuer of the P V MMAs
+//   warp  9    TMEM owner and MMA issuer: every MMA at d = 128; at d = 64
+//              the S MMAs (PVW) or every MMA of Q tile 0 (PTI)
+//   warp 10    d = 64: the P V MMAs (PVW) or every MMA of Q tile 1 (PTI)
 // Tensor memory (512 columns), d = 128: S_t at column 128 t (fp32 scores;
 // P_t is written back over its first 64 columns as packed bf16), O_t at
 // 256 + 128 t.  Issue order on the tensor pipe alternates the two tiles:
@@ -27,12 +27,15 @@
 // from S the order per key tile is S0(j+1) S1(j+1) | PV0(j) | PV1(j): S_t(j+1)
 // only waits until the softmax has read S_t(j) into registers, so it runs
 // while P_t(j) is computed, and the softmax waits for PV_t(j) (a commit of its
-// own) before it rewrites P_t or rescales O_t.  PVW (d = 64): the P V MMAs
-// come from a second issuing warp on another sub-partition (the S and P V
-// groups need no ordering between them), with K and V released separately;
-// one issuer cannot keep up with the softmax warpgroups that share its
-// sub-partition.  Measured faster for units of 8 or more key tiles and slower
-// for the short causal units of N <= 1024, so the launch picks it by shape.
+// own) before it rewrites P_t or rescales O_t.  One issuer cannot keep up
+// with the softmax warpgroups that share its sub-partition, so d = 64 has
+// two.  PVW: the P V MMAs come from a second warp on another sub-partition
+// (the S and P V groups need no ordering between them), with K and V
+// released separately.  PTI (short causal units, N < 2048): each Q tile has
+// an issuer of its own that moves on to the next unit as soon as its tile is
+// done, and the longer tile (one key tile more) alternates between the two
+// warpgroups from unit to unit, so that neither waits a tile at every unit
+// end; K / V slots take one release from each issuer.
 // F8 (d = 128): Q and K arrive as E4M3 codes (lensaml.com "FlashAttention",
 // "Key ideas", FlashAttention-3's FP8); each tile is one 128-byte-swizzled
 // block of 128 one-byte columns, S = Q K^T issues kind::f8f6f4 MMAs (K = 32
@@ -110,8 +113,8 @@ struct FwdBars {
   uint64_t* q_empty;   // [2][kQBufs]
   uint64_t* k_full;    // [S]
   uint64_t* v_full;    // [S]
-  uint64_t* kv_empty;  // [S] (PVW: K_j read)
-  uint64_t* v_empty;   // [S] PVW: V_j read
+  uint64_t* kv_empty;  // [S] (d = 64: K_j read; PTI: one release from each issuer)
+  uint64_t* v_empty;   // [S] d = 64: V_j read (PTI: one release from each issuer)
   uint64_t* s_full;    // [2]
   uint64_t* p_full;    // [2]
   uint64_t* o_full;    // [2]
@@ -158,19 +161,23 @@ __device__ __forceinline__ FwdUnit fwd_decode(int pos, int BH, int nqb, int N, i
 // DROP: dropout on the probabilities (fa_dropout.cuh): the row sum l keeps
 // every probability, the P fed to P V keeps only the surviving ones, and the
 // epilogue scales O by 1 / (1 - p).
-template <int D, bool CAUSAL, bool DROP, bool PVW, bool F8 = false>
+// ISSUE: 0 = one MMA warp, 1 = PVW (a second warp issues every P V),
+// 2 = PTI (one issuer per Q tile, d = 64; see the per-tile issuer below).
+template <int D, bool CAUSAL, bool DROP, int ISSUE, bool F8 = false>
 __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ lse, int BH, int N, float c2, DropParams dp, int* status) {
   using C = FwdCfg<D, F8>;
-  static_assert(!PVW || C::kSepP, "the P V warp needs P in columns of its own");
+  constexpr bool PVW = ISSUE == 1;
+  constexpr bool PTI = ISSUE == 2;
+  static_assert((PVW || PTI) == C::kSepP, "d = 64 takes two issuers (P in columns of its own), d = 128 one");
   // A negative scale arrives as a negative c2: the tensor core then computes
   // S negated (Q negated as the A operand) and everything after S uses |c2|,
   // so the row maximum and the masking below are those of a positive scale.
   const uint32_t s_negate = c2 < 0.f ? kIdescNegateA : 0u;
   c2 = fabsf(c2);
-  static_assert(!F8 || (D == 128 && !DROP && !PVW), "FP8 Q, K: d = 128, no dropout, one issuer");
+  static_assert(!F8 || (D == 128 && !DROP && ISSUE == 0), "FP8 Q, K: d = 128, no dropout, one issuer");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (!smem_base_ok(smem_raw, status)) return;
   uint8_t* sm = smem_raw;
@@ -199,6 +206,11 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
   const int total_units = BH * nqb;
   const int grid = gridDim.x;
   const bool block_major = block_major_order(CAUSAL, total_units, grid, N);
+  // The unit's Q tile that warpgroup / issuer t works on in round `round`:
+  // tile t, except with per-tile issuers under the causal mask, where the
+  // longer tile (the second one sees one key tile more) alternates between
+  // the two from round to round, so that neither runs a tile ahead for good.
+  auto slot_of = [](int t, int round) { return (PTI && CAUSAL) ? (t ^ (round & 1)) : t; };
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < 2 * C::kQBufs; ++q) {
@@ -215,10 +227,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&B.k_full[s], 1);
       mbar_init(&B.v_full[s], 1);
-      mbar_init(&B.kv_empty[s], 1);
-      mbar_init(&B.v_empty[s], 1);
+      mbar_init(&B.kv_empty[s], PTI ? 2 : 1);  // PTI: both tiles' issuers release each K / V slot
+      mbar_init(&B.v_empty[s], PTI ? 2 : 1);
     }
-    mbar_init(B.mma_done, PVW ? 2 : 1);
+    mbar_init(B.mma_done, (PVW || PTI) ? 2 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -253,7 +265,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
           tr(30);
           #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (t >= u.nq || !ok) continue;
+            const int sl = slot_of(t, round);  // the unit's Q tile for warpgroup t's buffers
+            if (sl >= u.nq || !ok) continue;
             const int qb = t * C::kQBufs + qcnt[t] % C::kQBufs;
             ok = mbar_wait(&B.q_empty[qb], ((qcnt[t] / C::kQBufs) & 1) ^ 1, status);
             tr(31);
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
             uint8_t* dst = sm + C::kOffQ + qb * C::kQKBytes;
             mbar_expect_tx(&B.q_full[qb], C::kQKBytes);
             for (int kb = 0; kb < C::kQKBlocks; ++kb)
-              tma_load_3d(dst + kb * kSwzBlockBytes, &tm_q, &B.q_full[qb], kb * C::kQKBlockCols, u.q0 + t * kTileRows,
+              tma_load_3d(dst + kb * kSwzBlockBytes, &tm_q, &B.q_full[qb], kb * C::kQKBlockCols, u.q0 + sl * kTileRows,
                           u.bh);
             ++qcnt[t];
           }
@@ -277,7 +290,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
             mbar_expect_tx(&B.k_full[st], C::kQKBytes);
             for (int kb = 0; kb < C::kQKBlocks; ++kb)
               tma_load_3d(kd + kb * kSwzBlockBytes, &tm_k, &B.k_full[st], kb * C::kQKBlockCols, j * kTileRows, u.bh);
-            if (PVW && !(ok = mbar_wait(&B.v_empty[st], ph ^ 1, status))) break;
+            if ((PVW || PTI) && !(ok = mbar_wait(&B.v_empty[st], ph ^ 1, status))) break;
             mbar_expect_tx(&B.v_full[st], C::kTileBytes);
             for (int kb = 0; kb < C::kBlocks; ++kb)
               tma_load_3d(vd + kb * kSwzBlockBytes, &tm_v, &B.v_full[st], kb * 64, j * kTileRows, u.bh);
@@ -297,7 +310,97 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
           mbar_wait(&B.v_full[i % C::kStages], (i / C::kStages) & 1, status);
         }
       }
-    } else if (warp == 9) {
+    } else if (PTI && (warp == 9 || warp == 10)) {
+      // ------------------------------------------------ per-tile issuers (PTI) --
+      // Warp 9 + w issues every MMA of warpgroup w: S_w(j+1) once the softmax
+      // has read S_w(j), P_w V_j once P_w(j) is written, in that order per
+      // tile, and moves on to the next unit as soon as its own tile is done.
+      // Each K / V slot is released by both issuers (two arrivals): the one
+      // whose tile skips key tile j waits until the slot holds it, so that its
+      // arrival cannot count towards the slot's previous use.
+      const int w = warp - 9;
+      const uint32_t idS = idesc_bf16(128, 128, 0, 0) | s_negate;  // S = (+/-) Q K^T, both K-major
+      constexpr uint32_t kIdescO = idesc_bf16(128, D, 0, 1);    // O += P V, V is MN-major
+      const uint32_t q_s = smem_addr(sm + C::kOffQ);
+      const uint32_t k_s = smem_addr(sm + C::kOffK);
+      const uint32_t v_s = smem_addr(sm + C::kOffV);
+      const uint32_t t_sw = tbase + C::kColS + 128 * w;
+      uint32_t qcnt = 0, pcnt = 0, sis = 0, kv_it = 0;
+      bool ok = true;
+      auto issue_s = [&](int st, int qb) -> bool {  // S_w into its columns, once the softmax read the last one
+        if (sis > 0 && !mbar_wait_warp(&B.s_free[w], (sis - 1) & 1, status)) return false;
+        tc_fence_after();
+        ++sis;
+        const uint32_t qa = q_s + qb * C::kQKBytes, ka = k_s + st * C::kQKBytes;
+#pragma unroll
+        for (int kb = 0; kb < D / 64; ++kb)
+          mma_ss_run_w<4, 2, 2>(t_sw, sdesc(qa + kb * kSwzBlockBytes, 16, 1024),
+                                sdesc(ka + kb * kSwzBlockBytes, 16, 1024), idS, kb > 0);
+        mma_commit_w(&B.s_full[w]);
+        return true;
+      };
+      for (int round = 0; ok; ++round) {
+        const int pos = snake_unit(round, blockIdx.x, grid);
+        if (round * grid >= total_units) break;
+        if (pos >= total_units) continue;
+        const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
+        const int sl = slot_of(w, round);
+        const int n = sl < u.nq ? u.nkv(sl) : 0;  // key tiles this tile visits
+        const int qb = w * C::kQBufs + qcnt % C::kQBufs;
+        if (n > 0) {
+          ok = mbar_wait_warp(&B.q_full[qb], (qcnt / C::kQBufs) & 1, status);
+          ++qcnt;
+        }
+        for (int j = 0; j < u.nkv_max && ok; ++j) {
+          const uint32_t it = kv_it + j;
+          const int st = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (j >= n) {  // key tile j is the other tile's alone: release this issuer's share of the slot
+            ok = mbar_wait_warp(&B.k_full[st], ph, status) && mbar_wait_warp(&B.v_full[st], ph, status);
+            if (!ok) break;
+            if (lane == 0) {
+              mbar_arrive(&B.kv_empty[st]);
+              mbar_arrive(&B.v_empty[st]);
+            }
+            __syncwarp();
+            continue;
+          }
+          if (j == 0) {
+            ok = mbar_wait_warp(&B.k_full[st], ph, status);
+            if (!ok) break;
+            tc_fence_after();
+            ok = issue_s(st, qb);
+            if (!ok) break;
+            if (n == 1) mma_commit_w(&B.q_empty[qb]);  // last S of the unit
+          }
+          if (j + 1 < n) {  // S_w(j+1)
+            const uint32_t it1 = it + 1;
+            ok = mbar_wait_warp(&B.k_full[it1 % C::kStages], (it1 / C::kStages) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            ok = issue_s(it1 % C::kStages, qb);
+            if (!ok) break;
+            if (j + 2 == n) mma_commit_w(&B.q_empty[qb]);  // last S of the unit
+          }
+          mma_commit_w(&B.kv_empty[st]);  // K_j: its S was issued before (this commit covers it)
+          // P_w V_j
+          ok = mbar_wait_warp(&B.p_full[w], pcnt & 1, status);
+          ++pcnt;
+          if (ok) ok = mbar_wait_warp(&B.v_full[st], ph, status);
+          if (!ok) break;
+          tc_fence_after();
+          mma_ts_run_w<8, 8, 128>(tbase + C::kColO + D * w, tbase + C::kColP + C::kPStride * w,
+                                  sdesc(v_s + st * C::kTileBytes, kSwzBlockBytes, 1024), kIdescO, j > 0);
+          mma_commit_w(&B.pv_done[w]);
+          mma_commit_w(&B.v_empty[st]);
+        }
+        kv_it += u.nkv_max;
+        if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit_w(B.mma_done);
+      mbar_wait_warp(B.mma_done, 0, status);
+    } else if (!PTI && warp == 9) {
       // ---------------------------------------------------------- MMA issuer --
       {  // whole warp, converged: waits are warp-wide, one elected lane issues
         const uint32_t idS = idesc_bf16(128, 128, 0, 0) | s_negate;  // S = (+/-) Q K^T, both K-major
@@ -386,55 +489,6 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
                 if (!ok) break;
                 if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
                 tr(24 + t);
-              }
-              if (ok) mma_commit_w(&B.kv_empty[st]);
-            }
-          } else if constexpr (C::kSepP) {
-            // Per key tile j: S_0(j+1), S_1(j+1) (each once the softmax has read
-            // S_t(j)), then P_t V_j for each tile once P_t(j) is written.
-            for (int j = 0; j < u.nkv_max && ok; ++j) {
-              const uint32_t it = kv_it + j;
-              const int st = it % C::kStages;
-              const int st_next = (it + 1) % C::kStages;
-              bool k_next_ready = false;
-  #pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                if (t >= u.nq || j + 1 >= u.nkv(t) || !ok) continue;
-                if (!k_next_ready) {
-                  ok = mbar_wait_warp(&B.k_full[st_next], ((it + 1) / C::kStages) & 1, status);
-                  if (!ok) break;
-                  tc_fence_after();
-                  k_next_ready = true;
-                }
-                tr(40 + t);
-                ok = issue_s(t, st_next);
-                if (!ok) break;
-                if (j + 2 == u.nkv(t)) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
-                tr(24 + t);
-              }
-              if (!ok) break;
-              bool v_ready = false;
-  #pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                if (t >= u.nq || j >= u.nkv(t) || !ok) continue;
-                tr(20 + t);
-                ok = mbar_wait_warp(&B.p_full[t], pcnt[t] & 1, status);
-                tr(22 + t);
-                ++pcnt[t];
-                if (!ok) break;
-                if (!v_ready) {
-                  ok = mbar_wait_warp(&B.v_full[st], (it / C::kStages) & 1, status);
-                  if (!ok) break;
-                  v_ready = true;
-                }
-                tr(26 + t);
-                tc_fence_after();
-                const uint32_t va = v_s + st * C::kTileBytes;
-                // 16 keys a step: 8 P columns, 16 rows (2048 bytes) of V
-                mma_ts_run_w<8, 8, 128>(tbase + C::kColO + D * t, tbase + C::kColP + C::kPStride * t,
-                                      sdesc(va, kSwzBlockBytes, 1024), kIdescO, j > 0);
-                mma_commit_w(&B.pv_done[t]);
-                tr(28 + t);
               }
               if (ok) mma_commit_w(&B.kv_empty[st]);
             }
@@ -552,12 +606,13 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
       if (round * grid >= total_units) break;
       if (pos >= total_units) continue;
       const FwdUnit u = fwd_decode(pos, BH, nqb, N, nkv_total, CAUSAL, block_major);
-      if (t >= u.nq) continue;
-      const int qi = u.q0 + t * kTileRows + r;  // this thread's query row
-      const int jdiag = (u.q0 + t * kTileRows) / kTileRows;
+      const int sl = slot_of(t, round);  // the unit's Q tile this warpgroup works on
+      if (sl >= u.nq) continue;
+      const int qi = u.q0 + sl * kTileRows + r;  // this thread's query row
+      const int jdiag = (u.q0 + sl * kTileRows) / kTileRows;
       float m_run = -INFINITY;  // running max used by the exponentials (log2 units)
       float l_run = 0.f;        // running normaliser relative to m_run
-      for (int j = 0; j < u.nkv(t); ++j) {
+      for (int j = 0; j < u.nkv(sl); ++j) {
         tr(1);
         ok = mbar_wait_warp(&B.s_full[t], scnt & 1, status);
         tr(2);
@@ -725,10 +780,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool DROP, bool PVW = false, bool F8 = false>
+template <int D, bool CAUSAL, bool DROP, int ISSUE = 0, bool F8 = false>
 static cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   using C = FwdCfg<D, F8>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, DROP, PVW, F8>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, DROP, ISSUE, F8>;
   // The register split inside the kernel assumes it was built with exactly
   // kLaunchRegs registers a thread: with fewer, the softmax warpgroups' request
   // for more could never be met.  Refuse to launch such a build.
@@ -745,23 +800,24 @@ static cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// d = 64: the P V warp for units of 8 or more key tiles (N >= 1024), except
-// short causal units (causal N < 2048), where the single issuer measured faster.
-static bool use_pv_warp(const FwdLaunch& a) { return a.d == 64 && a.N >= 1024 && !(a.causal && a.N < 2048); }
-
+// d = 64: per-tile issuers for the short causal units (N < 2048: one to
+// fifteen key tiles per Q tile), the P V warp otherwise; each measured the
+// faster of the two (and of one issuer) on those shapes.
 template <int D, bool DROP>
 static cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t stream) {
   if constexpr (D == 64) {
-    if (use_pv_warp(a))
-      return a.causal ? launch_fwd_t<64, true, DROP, true>(a, stream) : launch_fwd_t<64, false, DROP, true>(a, stream);
+    if (a.causal)
+      return a.N < 2048 ? launch_fwd_t<64, true, DROP, 2>(a, stream) : launch_fwd_t<64, true, DROP, 1>(a, stream);
+    return launch_fwd_t<64, false, DROP, 1>(a, stream);
+  } else {
+    return a.causal ? launch_fwd_t<D, true, DROP>(a, stream) : launch_fwd_t<D, false, DROP>(a, stream);
   }
-  return a.causal ? launch_fwd_t<D, true, DROP>(a, stream) : launch_fwd_t<D, false, DROP>(a, stream);
 }
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
   if (a.fp8)  // E4M3 Q and K, d = 128 (checked by the caller)
-    return a.causal ? launch_fwd_t<128, true, false, false, true>(a, stream)
-                    : launch_fwd_t<128, false, false, false, true>(a, stream);
+    return a.causal ? launch_fwd_t<128, true, false, 0, true>(a, stream)
+                    : launch_fwd_t<128, false, false, 0, true>(a, stream);
   if (a.dropout) return a.d == 64 ? launch_fwd_d<64, true>(a, stream) : launch_fwd_d<128, true>(a, stream);
   return a.d == 64 ? launch_fwd_d<64, false>(a, stream) : launch_fwd_d<128, false>(a, stream);
 }
