@@ -89,12 +89,13 @@ int device_info(DeviceInfo* out) {
   return FA_OK;
 }
 
-// [B*H, N, d] bf16 viewed as a 3-D tensor; 128-row x 64-column boxes,
-// 128-byte swizzle (the layout the tcgen05 descriptors expect).
-int make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+// [B*H, N, d] bf16 viewed as a 3-D tensor; box_rows-row x 64-column boxes
+// (128 unless given), 128-byte swizzle (the layout the tcgen05 descriptors
+// expect).
+int make_map(CUtensorMap* m, const void* base, int BH, int N, int d, unsigned box_rows = 128) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -176,9 +177,15 @@ int run_forward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap&
                 int N, int d, int causal, float c2, const DeviceInfo& dev, int fp8, int dropout, const DropParams& drop,
                 cudaStream_t stream) {
   FwdLaunch a;
+  // The output in 32-row boxes, one per softmax warp, for the kernels that
+  // store O with TMA (d = 64, N < 4096); the others never read the map.
+  CUtensorMap to;
+  const bool o_map = d == 64 && !fp8 && N < 4096;
+  if (o_map && make_map(&to, o, BH, N, d, 32)) return FA_ERR_CUDA;
   a.tm_q = &tq;
   a.tm_k = &tk;
   a.tm_v = &tv;
+  a.tm_o = o_map ? &to : &tq;
   a.o = o;
   a.lse = lse;
   a.BH = BH;

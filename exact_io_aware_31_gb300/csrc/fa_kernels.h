@@ -13,6 +13,7 @@ struct FwdLaunch {
   const CUtensorMap* tm_q;
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_v;
+  const CUtensorMap* tm_o;  // bf16 [BH, N, d] output, 64-column x 32-row boxes (stored with TMA at d = 64)
   void* o;
   float* lse;
   int BH, N, d;
