@@ -123,8 +123,8 @@ struct FwdBars {
   uint64_t* q_empty;   // [2][kQBufs]
   uint64_t* k_full;    // [S]
   uint64_t* v_full;    // [S]
-  uint64_t* kv_empty;  // [S] (d = 64: K_j read; PTI: one release from each issuer)
-  uint64_t* v_empty;   // [S] d = 64: V_j read (PTI: one release from each issuer)
+  uint64_t* kv_empty;  // [S] K_j read (PTI: one release from each issuer)
+  uint64_t* v_empty;   // [S] V_j read (PTI: one release from each issuer)
   uint64_t* s_full;    // [2]
   uint64_t* p_full;    // [2]
   uint64_t* o_full;    // [2]
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8, EPI>::kThreads, 1)
             mbar_expect_tx(&B.k_full[st], C::kQKBytes);
             for (int kb = 0; kb < C::kQKBlocks; ++kb)
               tma_load_3d(kd + kb * kSwzBlockBytes, &tm_k, &B.k_full[st], kb * C::kQKBlockCols, j * kTileRows, u.bh);
-            if ((PVW || PTI) && !(ok = mbar_wait(&B.v_empty[st], ph ^ 1, status))) break;
+            if (!(ok = mbar_wait(&B.v_empty[st], ph ^ 1, status))) break;  // K and V slots are released apart
             mbar_expect_tx(&B.v_full[st], C::kTileBytes);
             for (int kb = 0; kb < C::kBlocks; ++kb)
               tma_load_3d(vd + kb * kSwzBlockBytes, &tm_v, &B.v_full[st], kb * 64, j * kTileRows, u.bh);
@@ -477,6 +477,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8, EPI>::kThreads, 1)
               if (t < u.nq && ok && u.nkv(t) == 1) mma_commit_w(&B.q_empty[qbuf[t]]);  // last S_t of the unit
             }
             if (!ok) break;
+            if constexpr (ISSUE == 0) mma_commit_w(&B.kv_empty[st]);  // K_0 read by both S_t(0)
           }
           if constexpr (PVW) {
             // Per key tile j: S_0(j+1), S_1(j+1), each once the softmax has read
@@ -546,7 +547,15 @@ __global__ void __launch_bounds__(FwdCfg<D, F8, EPI>::kThreads, 1)
               }
               tr(24 + t);
             }
-            if (ok) mma_commit_w(&B.kv_empty[st]);
+            // V_j is read by both P_t V_j; K_{j+1} by both S_t(j+1), issued
+            // here: its slot goes back to the producer a key tile earlier
+            // than V_j's, so the copy of K_{j+3} has two key tiles of lead
+            // (with one ring of two shared slots the MMA warp waited for
+            // K_{j+1} about 1250 cycles a key tile, traced).
+            if (ok) {
+              mma_commit_w(&B.v_empty[st]);
+              if (j + 1 < u.nkv_max) mma_commit_w(&B.kv_empty[st_next]);
+            }
           }
           kv_it += u.nkv_max;
           if (__any_sync(0xffffffffu, aborted(abort_flag))) ok = false;
