@@ -37,11 +37,9 @@ __host__ __device__ inline int snake_unit(int round, int cta, int grid) {
 // GB300, block-major wins for causal N >= 4096 with few units per CTA (B = 1,
 // H = 32, d = 128 forward: 0.130 -> 0.110 ms) and loses at N = 1024, where
 // locality matters more (B = 16, H = 16, d = 128: 0.089 -> 0.098 ms).
-#ifndef FA_BLOCK_MAJOR_MIN_N
-#define FA_BLOCK_MAJOR_MIN_N 4096  // tuning knob
-#endif
+constexpr int kBlockMajorMinN = 4096;
 __host__ __device__ inline bool block_major_order(bool causal, int total_units, int grid, int N) {
-  return causal && N >= FA_BLOCK_MAJOR_MIN_N && total_units < 16 * grid;
+  return causal && N >= kBlockMajorMinN && total_units < 16 * grid;
 }
 
 // Schedule position -> (slice bh, block index within the slice, 0 = first).

@@ -59,15 +59,13 @@ namespace fa {
 static __device__ int g_fa_test_withhold_arrival;
 #endif
 
-// Tuning knob: K/V ring depth at d = 64 (3 to 5 fit in shared memory; 3, 4
-// and 5 measured within 2% of each other).
-#ifndef FA_FWD_STAGES_D64
-#define FA_FWD_STAGES_D64 4
-#endif
+// K / V ring depth at d = 64 (3, 4 and 5 slots measured within 2% of each
+// other; 4 leaves room for the TMA-store epilogue's staging boxes).
+constexpr int kFwdStagesD64 = 4;
 
 template <int D, bool F8 = false, bool EPI = false>
 struct FwdCfg {
-  static constexpr int kStages = (D == 128) ? 2 : FA_FWD_STAGES_D64;
+  static constexpr int kStages = (D == 128) ? 2 : kFwdStagesD64;
   static constexpr int kQBufs = (D == 128) ? 1 : 2;  // Q buffers per tile (next unit's Q prefetched at d = 64)
   static constexpr int kTileBytes = kTileRows * D * 2;  // a bf16 tile (V; Q and K unless F8)
   static constexpr int kBlocks = D / 64;                // its 128-byte-swizzled 64-column blocks
