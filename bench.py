@@ -206,10 +206,19 @@ def oracle_units(w):
     return units
 
 
-def oracle_unit_flops(w, rows):
-    """The metric's FLOPs (fwd + bwd) carried by `rows` query rows of one slice."""
+def oracle_unit_flops(w, r0, rows):
+    """The metric's FLOPs (fwd + bwd) carried by query rows r0 .. r0 + rows - 1 of one slice.
+
+    A slice's FLOPs are shared out in proportion to the (query, key) pairs each
+    row covers: all N keys, or under the causal mask keys 0 .. i for row i,
+    so a sample of early (light) and late (heavy) row blocks is credited
+    with the work it really did."""
     fwd, bwd = flops_per_step(w)
-    return (fwd + bwd) * rows / (w.B * w.H * w.N)
+    per_slice = (fwd + bwd) / (w.B * w.H)
+    if not w.causal:
+        return per_slice * rows / w.N
+    pairs = rows * r0 + rows * (rows + 1) // 2  # sum of (i + 1) over the rows
+    return per_slice * pairs / (w.N * (w.N + 1) // 2)
 
 
 def oracle_run_unit(w, q, k, v, do, unit):
@@ -229,7 +238,7 @@ def oracle_sample(w, q, k, v, do, seconds, start=0):
     while True:
         unit = units[(start + done) % len(units)]
         oracle_run_unit(w, q, k, v, do, unit)
-        flops += oracle_unit_flops(w, unit[3])
+        flops += oracle_unit_flops(w, unit[2], unit[3])
         done += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -263,7 +272,7 @@ def run_reference(args, w):
         el = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(el)
-            flops.append(oracle_unit_flops(w, unit[3]))
+            flops.append(oracle_unit_flops(w, unit[2], unit[3]))
     value = sum(flops) / sum(times) / 1e12
     fwd, bwd = flops_per_step(w)
     ms = 1e3 * sum(times) / len(times)
